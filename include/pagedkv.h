@@ -1,0 +1,248 @@
+/*
+ * pagedkv.h - C ABI of libpagedkv.so: paged KV-cache data movement on one GB300 (sm_103a).
+ *
+ * The library moves paged KV-cache bytes the way a prefill/decode-disaggregated
+ * vLLM deployment does on each GPU:
+ *   1. kv_slot_mapping + kv_reshape_and_cache   write new tokens' K/V into the paged
+ *                                               per-layer caches;
+ *   2. kv_build_xfer_list                       flatten per-request block lists into
+ *                                               maximal contiguous block runs;
+ *   3. kv_pack_blocks                           gather those runs into one contiguous
+ *                                               staging buffer (the sender's payload);
+ *   4. kv_unpack_blocks                         scatter a staging buffer into the
+ *                                               receiver's own block ids, optionally
+ *                                               with another block size or a head slice.
+ * The network transfer between machines is not part of this library.
+ *
+ * Conventions for every entry point
+ *  - Pointers named "device" are caller-owned CUDA device memory; the library never
+ *    allocates, frees or keeps them.  Host arrays (kv_cache_desc.base, the new_kv
+ *    pointer table) are read during the call only.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronises, except kv_get_last_error.
+ *  - Payload bytes are opaque: rows are moved as 16-byte vectors and never converted,
+ *    so NaN payloads, infinities and -0 arrive bit-exact.
+ *  - Argument errors the host can see are returned at once and nothing is launched.
+ *    Data-dependent errors (an id or slot outside the cache, a list inconsistent with
+ *    its offsets) skip only the offending write and set a bit in a sticky per-device
+ *    error word, read and cleared with kv_get_last_error.
+ *  - Base addresses, strides, row and slice sizes and staging pointers must be multiples
+ *    of 16 bytes (KV_ERR_ALIGN otherwise).
+ *
+ * Sources (the vLLM PD-disaggregation pages this library restates):
+ *  [S] drawing "vllm v1 调度逻辑 和 distributed 分布式原理": "batch tensor 组装" (the slot
+ *      formula), "Paged kv cache" (16 slots per block), "总的就是 all kv cache" (one
+ *      tensor per layer, one block_table for all layers) and the two layer shapes.
+ *  [N] page "0. vllm 如何使用 nccl 传输 kv cache", sections 2.3 (transfer flow) and 2.4
+ *      (extract_kv_from_layer / inject_kv_into_layer).
+ *  [F] page "5. flagcx connector design & dev & test", section 1.2 (xfer_list "per layer
+ *      x per contiguous group x per req").
+ *  [M] page "vLLM PD 分离 源码级机制", sections 4.1 (receiver metadata: base addresses,
+ *      block lengths, local block ids) and 4.2 (_build_transfer_params, _send_blocks).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are the only symbols libpagedkv.so exports. */
+#if defined(__GNUC__)
+#define KV_API __attribute__((visibility("default")))
+#else
+#define KV_API
+#endif
+
+typedef struct CUstream_st *kv_stream_t; /* identical to cudaStream_t */
+
+/* Status codes returned by every entry point. */
+enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent descriptor */
+    KV_ERR_ALIGN = 2,       /* an address, stride or size is not a multiple of 16 bytes */
+    KV_ERR_RANGE = 3,       /* a size does not fit: slice beyond the row, staging too small */
+    KV_ERR_CUDA = 4,        /* a CUDA runtime call failed (see kv_last_cuda_error) */
+    KV_ERR_TIMEOUT = 5,     /* a bounded device wait gave up */
+    KV_ERR_UNSUPPORTED = 6  /* outside the implemented limits (documented per call) */
+};
+
+/* Bits of the sticky device error word (kv_get_last_error). */
+#define KV_DERR_TABLE     0x01 /* slot_mapping: request, position or table entry invalid (slot -1 written) */
+#define KV_DERR_SLOT      0x02 /* reshape_and_cache: slot beyond num_blocks * block_size (row skipped) */
+#define KV_DERR_BLOCK     0x04 /* pack/unpack: a run names a block outside the cache (run skipped) */
+#define KV_DERR_LIST      0x08 /* xfer builder: req_offsets[0] != 0 or req_offsets[n_reqs] != n_blocks */
+#define KV_DERR_CAPACITY  0x10 /* more runs than run_capacity (extra runs not written / not copied) */
+#define KV_DERR_STAGE     0x20 /* a run's staging range lies outside the staging buffer (run skipped) */
+#define KV_DERR_DST_TABLE 0x40 /* unpack remap: a request's destination list is too short (rows skipped) */
+#define KV_DERR_TIMEOUT   0x80 /* a bounded device wait gave up */
+
+/*
+ * Geometry of one paged cache [S][M].  A cache is n_tensors device tensors of equal
+ * geometry (one per layer, or one K and one V tensor per layer).  Row (t, b, p, o) -
+ * tensor t, block b, plane p (0 = K, 1 = V when a tensor holds both), slot o - starts at
+ *     base[t] + b * block_stride + p * plane_stride + o * token_stride
+ * and holds row_bytes bytes (heads * head_dim * element size).  Examples:
+ *     separate K/V [num_blocks, bs, H, D]:  n_planes 1, block_stride bs*row, token_stride row
+ *     blocks-first [num_blocks, 2, bs, H, D]: n_planes 2, plane_stride bs*row, block_stride 2*bs*row
+ *     kv-first     [2, num_blocks, bs, H, D]: n_planes 2, plane_stride num_blocks*bs*row
+ *     MLA latent   [num_blocks, bs, 576]:    n_planes 1, row 1152
+ * base is a HOST array of n_tensors device addresses; it is read during the call only.
+ */
+typedef struct {
+    int32_t n_tensors;
+    int32_t block_size;   /* token slots per block (> 0) */
+    int32_t n_planes;     /* 1 or 2 */
+    int32_t row_bytes;    /* bytes of one token row of one plane */
+    int64_t num_blocks;   /* blocks per tensor */
+    int64_t block_stride; /* bytes */
+    int64_t plane_stride; /* bytes (ignored when n_planes == 1) */
+    int64_t token_stride; /* bytes */
+    const uint64_t *base; /* host array [n_tensors] of device addresses */
+} kv_cache_desc;
+
+/*
+ * Layout of a staging buffer [N][F].  Staged entry (t, i, p, o) - tensor t, entry i of
+ * the flattened block list (requests in order, each request's blocks in list order),
+ * plane p, slot o of the source block size - is slice_bytes bytes at
+ *     ((((t * n_blocks + i) * n_planes + p) * block_size) + o) * slice_bytes.
+ * For a whole-row slice this is layer[block_ids] per (request, tensor) concatenated,
+ * i.e. the tensor the NCCL connector sends per "request_id#layer_name" [N].
+ */
+typedef struct {
+    int64_t n_blocks;    /* N: entries in the flattened source block list */
+    int32_t n_tensors;
+    int32_t n_planes;
+    int32_t block_size;  /* SOURCE block size */
+    int32_t slice_bytes; /* bytes per staged row (multiple of 16) */
+} kv_stage_desc;
+
+/* One contiguous group [F][M]: n_blocks consecutive source ids starting at src_block,
+ * landing on consecutive destination ids starting at dst_block (-1 when the list had no
+ * destination ids), occupying staging entries stage_block .. stage_block + n_blocks - 1.
+ * 24 bytes, 8-byte aligned. */
+typedef struct {
+    int32_t req;
+    int32_t src_block;
+    int32_t dst_block;
+    int32_t n_blocks;
+    int64_t stage_block;
+} kv_xfer_run;
+
+/* Library version string, e.g. "pagedkv 0.1.0 sm_103a". */
+KV_API const char *kv_version(void);
+
+/* Human-readable name of a status code. */
+KV_API const char *kv_status_string(int status);
+
+/* The last CUDA runtime error seen by a call that returned KV_ERR_CUDA (cudaError_t value). */
+KV_API int kv_last_cuda_error(void);
+
+/*
+ * kv_slot_mapping [S "batch tensor 组装"]:
+ *     slot_out[i] = block_table[token_req[i] * bt_row_stride + token_pos[i] / block_size] * block_size
+ *                   + token_pos[i] % block_size
+ * block_table: device int32 [n_reqs, max_blocks_per_req] with row stride bt_row_stride
+ * (elements); token_req, token_pos: device int32 [n_tokens]; slot_out: device int64
+ * [n_tokens].  A token whose request is outside [0, n_reqs), whose position is negative
+ * or beyond max_blocks_per_req * block_size, or whose table entry is negative gets
+ * slot -1 and sets KV_DERR_TABLE.  n_tokens == 0 launches nothing.
+ */
+KV_API int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t max_blocks_per_req,
+                    int64_t bt_row_stride, const int32_t *token_req, const int32_t *token_pos,
+                    int64_t n_tokens, int32_t block_size, int64_t *slot_out, kv_stream_t stream);
+
+/*
+ * kv_reshape_and_cache [S "Paged kv cache", M timeline "KV Cache 写入本地显存"]:
+ * for every cache tensor t, plane p and token i with slot[i] >= 0,
+ *     row (t, slot[i] / block_size, p, slot[i] % block_size) <- new_kv[t * n_planes + p] + i * new_token_stride
+ * All tensors of the descriptor (e.g. every layer of a decode step) are written by one
+ * launch per 128 tensors.  new_kv: HOST array of n_tensors * n_planes device addresses,
+ * each of [n_tokens] rows of cache->row_bytes bytes, new_token_stride bytes apart.
+ * slot: device int64 [n_tokens]; slot < 0 is a padding token and is skipped; a slot at
+ * or beyond num_blocks * block_size sets KV_DERR_SLOT and is skipped.  Two tokens with
+ * the same slot race (undefined which row lands).  Limits: num_blocks * block_size
+ * < 2^31 and n_tokens * n_planes * row_bytes / 16 < 2^31 (KV_ERR_UNSUPPORTED).
+ */
+KV_API int kv_reshape_and_cache(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride,
+                         const int64_t *slot, int64_t n_tokens, kv_stream_t stream);
+
+/* Device workspace bytes kv_build_xfer_list needs for a list of n_blocks entries. */
+KV_API int kv_xfer_workspace_bytes(int64_t n_blocks, int64_t *bytes_out);
+
+/*
+ * kv_build_xfer_list [F section 1.2, M section 4.2]: flattens per-request block lists
+ * into runs, in request order then list order.  Entry i starts a new run when it is
+ * the first entry of its request, when src_ids[i] != src_ids[i-1] + 1, when dst_ids
+ * is given and dst_ids[i] != dst_ids[i-1] + 1, or when the open run already holds
+ * max_run_blocks blocks (max_run_blocks > 0; 0 = uncapped).  Ids keep their list
+ * order; nothing is sorted.
+ * req_offsets: device int32 [n_reqs + 1] (CSR: request r owns entries
+ * [req_offsets[r], req_offsets[r+1]), req_offsets[0] = 0, req_offsets[n_reqs] =
+ * n_blocks); src_ids, dst_ids: device int32 [n_blocks], dst_ids may be NULL.
+ * Output: runs (device, run_capacity records) and *n_runs (device int32, the total
+ * number of runs, even when it exceeds run_capacity, in which case KV_DERR_CAPACITY is
+ * set and only the first run_capacity runs are written; n_blocks runs always suffice).
+ * workspace: device scratch of kv_xfer_workspace_bytes(n_blocks) bytes, 16-byte
+ * aligned, zeroed by this call on `stream`; calls sharing a workspace must be ordered.
+ * Limit: n_blocks < 2^31 - 2^12.
+ */
+KV_API int kv_build_xfer_list(const int32_t *req_offsets, int32_t n_reqs, const int32_t *src_ids,
+                       const int32_t *dst_ids, int64_t n_blocks, int32_t max_run_blocks,
+                       kv_xfer_run *runs, int64_t run_capacity, int32_t *n_runs,
+                       void *workspace, int64_t workspace_bytes, kv_stream_t stream);
+
+/*
+ * kv_pack_blocks [N section 2.4 extract_kv_from_layer, F section 1.2]: for every
+ * tensor t and run of `runs`, copies rows (t, src_block + m, p, o) - byte slice
+ * [src_slice_off, src_slice_off + stage->slice_bytes) of each row - to the staging
+ * entries (t, stage_block + m, p, o) of the layout in kv_stage_desc.
+ * stage->n_tensors, n_planes and block_size must equal the cache's.  runs/n_runs are
+ * device memory as written by kv_build_xfer_list; at most run_capacity runs are read
+ * (KV_DERR_CAPACITY if *n_runs is larger).  max_run_blocks is the cap the runs were
+ * built with (0 if uncapped): runs are split into pieces of at most 16 KiB for the
+ * warps by it; a longer run is still copied whole.  stage: device, stage_bytes bytes, at least
+ * n_tensors * n_blocks * n_planes * block_size * slice_bytes.  A run outside the cache
+ * (KV_DERR_BLOCK) or the staging range (KV_DERR_STAGE) is skipped.
+ */
+KV_API int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const kv_stage_desc *stage,
+                   const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
+                   int32_t max_run_blocks, void *stage_buf, int64_t stage_bytes, kv_stream_t stream);
+
+/*
+ * kv_unpack_blocks [N section 2.3 step 14 (kv_cache_layer[block_ids] = tensor),
+ * M sections 4.1-4.2 (receiver block ids, TP heterogeneity)]: the inverse of pack, into
+ * the receiver's cache `dst`, writing each staged row slice at byte dst_slice_off of the
+ * destination row (stage->slice_bytes bytes).
+ *  - Whole-block mode (dst_ids == NULL): staged block stage_block + m of each run goes to
+ *    destination block dst_block + m (runs built with destination ids).  Needs
+ *    stage->block_size == dst->block_size.
+ *  - Remap mode (dst_ids != NULL): staged token j of request r (j counts the slots of r's
+ *    staged blocks in order) goes to slot j % dst->block_size of block
+ *    dst_ids[dst_req_offsets[r] + j / dst->block_size].  src_req_offsets is the CSR the
+ *    runs were built from; dst_req_offsets/dst_ids the receiver's per-request block
+ *    lists (device int32, n_reqs + 1 and any length).  A request whose destination list
+ *    is too short sets KV_DERR_DST_TABLE and its uncovered rows are skipped.
+ * max_run_blocks: as for kv_pack_blocks.
+ * stage->n_tensors and n_planes must equal dst's.  Destination ids must be distinct:
+ * two staged rows aimed at one destination row race.
+ */
+KV_API int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
+                     const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
+                     int32_t max_run_blocks, const void *stage_buf, int64_t stage_bytes,
+                     const int32_t *src_req_offsets, const int32_t *dst_req_offsets,
+                     const int32_t *dst_ids, int32_t n_reqs, kv_stream_t stream);
+
+/*
+ * kv_get_last_error: copies the current device's sticky error word (KV_DERR_* bits) to
+ * *host_out after the work queued on `stream` so far, clears it when clear != 0, and
+ * SYNCHRONISES `stream`.  Work on other streams is not waited for.
+ */
+KV_API int kv_get_last_error(int32_t *host_out, int32_t clear, kv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -1,0 +1,92 @@
+// Internal helpers shared by the libpagedkv translation units (not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// Cache tensors whose base addresses one launch carries in its parameter block.
+constexpr int kMaxTensorsPerLaunch = 128;
+
+// ---------------------------------------------------------------------------
+// Unsigned 32-bit division by a runtime-invariant divisor with a multiply and a
+// shift (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, section 4): for 1 <= d < 2^31 and l = ceil(log2 d),
+// m = floor(2^32 * (2^l - d) / d) + 1 and q = (mulhi(n, m) + n) >> l for every
+// 32-bit n.  The sum is formed in 64 bits so it cannot overflow.
+// ---------------------------------------------------------------------------
+struct FastDiv {
+    uint32_t d;
+    uint32_t m;
+    uint32_t l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f{d, 0u, 0u};
+    while ((1ull << f.l) < d) f.l++;
+    f.m = (uint32_t)(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+    return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f)
+{
+#ifdef __CUDA_ARCH__
+    uint32_t hi = __umulhi(n, f.m);
+#else
+    uint32_t hi = (uint32_t)(((uint64_t)n * f.m) >> 32);
+#endif
+    return (uint32_t)(((uint64_t)hi + n) >> f.l);
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte global accesses.  Cache rows are read once (no L1 allocation); staging
+// and cache writes are streaming (evict-first) stores.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_once(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void set_error(int *err, int bits)
+{
+    atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Host-side runtime state (kv_runtime.cu).
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int *err_word;  // device address of this device's sticky error word
+};
+
+// Info of the current device, created on first use; nullptr after a CUDA error
+// (the error is recorded for kv_last_cuda_error).
+const DeviceInfo *current_device();
+
+// Records a CUDA error and returns KV_ERR_CUDA, or KV_OK for cudaSuccess.
+int cuda_status(cudaError_t e);
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+inline bool aligned16(int64_t v) { return (v & 15) == 0; }
+
+// Validates a cache descriptor; checks the tensor base addresses too.
+int check_cache(const kv_cache_desc *c);
+
+}  // namespace pkv

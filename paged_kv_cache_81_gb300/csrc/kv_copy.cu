@@ -1,0 +1,349 @@
+// kv_pack_blocks / kv_unpack_blocks: the gather into, and scatter out of, the staging buffer.
+//
+// Gather semantics: page "0. vllm 如何使用 nccl 传输 kv cache", section 2.4
+// (extract_kv_from_layer: layer[block_ids] / layer[:, block_ids]); scatter semantics: the
+// same page, section 2.3 step 14 (kv_cache_layer[block_ids] = tensor); per-layer,
+// per-block addressing with a head slice for TP heterogeneity: page "vLLM PD 分离 源码级
+// 机制", section 4.2 (_build_transfer_params).
+//
+// Work decomposition: an item is one piece (at most kPieceChunks 16-byte chunks) of one
+// (tensor, run).  Items are numbered tensor-major, so consecutive warps write adjacent
+// staging ranges; the grid is persistent (resident CTAs on every SM) and walks the items
+// with a warp stride.  Inside a piece each lane keeps kUnroll 16-byte loads in flight
+// before storing them.
+//
+// Address modes of the cache side (the staging side is always linear):
+//   MERGED  a run is one contiguous span (dense blocks, block_stride == staged block bytes)
+//   BLOCKS  each block is contiguous but blocks are block_stride apart
+//   ROWS    row by row: a head slice, a strided token dimension, or kv-first planes
+//   REMAP   unpack onto another block size / another block list (token granular)
+#include <algorithm>
+#include <mutex>
+
+#include "kv_common.cuh"
+
+namespace {
+
+using pkv::FastDiv;
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 8;
+constexpr uint32_t kPieceChunks = 1024;  // 16 KiB
+
+enum Mode { MERGED = 0, BLOCKS = 1, ROWS = 2, REMAP = 3 };
+
+struct CopyParams {
+    const kv_xfer_run *runs;
+    const int32_t *n_runs;
+    int64_t run_capacity;
+    uint8_t *stage;
+    int64_t stage_tensor_bytes;  // n_stage_blocks * stage_block_bytes
+    int64_t stage_block_bytes;   // planes * bs * slice
+    int64_t n_stage_blocks;
+    int64_t num_blocks;  // cache blocks per tensor
+    int64_t block_stride;
+    int64_t plane_stride;
+    int64_t token_stride;
+    int32_t row_off;  // byte offset of the slice inside a cache row
+    int32_t n_tensors;
+    int32_t tensor_begin;
+    int32_t max_pieces;
+    uint32_t chunks_per_block;  // staged block / 16
+    FastDiv div_cpr;            // chunks per staged row
+    FastDiv div_bs;             // staged (source) block size
+    FastDiv div_rpb;            // staged rows per block = planes * bs
+    FastDiv div_cpb;            // chunks per staged block
+    FastDiv div_dbs;            // destination block size (REMAP)
+    const int32_t *src_req_offsets;
+    const int32_t *dst_req_offsets;
+    const int32_t *dst_ids;
+    int32_t n_reqs;
+    int *err;
+    uint64_t base[pkv::kMaxTensorsPerLaunch];
+};
+
+template <int MODE, bool PACK>
+__global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_constant__ CopyParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    int64_t nr = *p.n_runs;
+    if (nr > p.run_capacity) {
+        if (warp == 0 && lane == 0) pkv::set_error(p.err, KV_DERR_CAPACITY);
+        nr = p.run_capacity;
+    }
+    if (nr < 0) nr = 0;
+    const int64_t per_tensor = nr * p.max_pieces;
+    const int64_t items = per_tensor * p.n_tensors;
+
+    for (int64_t item = warp; item < items; item += n_warps) {
+        const int32_t t = (int32_t)(item / per_tensor);
+        const int64_t rest = item - (int64_t)t * per_tensor;
+        const int64_t k = rest / p.max_pieces;
+        const int32_t piece = (int32_t)(rest - k * p.max_pieces);
+        const kv_xfer_run run = p.runs[k];
+
+        const uint64_t item_chunks64 = (uint64_t)(int64_t)run.n_blocks * p.chunks_per_block;
+        const uint64_t c_begin = (uint64_t)piece * kPieceChunks;
+        if (run.n_blocks <= 0 || c_begin >= item_chunks64) continue;
+        const bool first_piece = piece == 0;
+        if (run.stage_block < 0 || run.stage_block + run.n_blocks > p.n_stage_blocks ||
+            item_chunks64 >= (1ull << 32)) {
+            if (first_piece && lane == 0) pkv::set_error(p.err, KV_DERR_STAGE);
+            continue;
+        }
+        const uint32_t item_chunks = (uint32_t)item_chunks64;
+        const uint32_t c_end =
+            piece == p.max_pieces - 1 ? item_chunks : (uint32_t)std::min<uint64_t>(c_begin + kPieceChunks, item_chunks);
+
+        int64_t blk = 0;  // first cache block of the run (MERGED / BLOCKS / ROWS)
+        int32_t j0 = 0, dn = 0;  // REMAP: first staged token of the run in its request; dst list length
+        const int32_t *dl = nullptr;
+        if (MODE == REMAP) {
+            const int32_t r = run.req;
+            if (r < 0 || r >= p.n_reqs) {
+                if (first_piece && lane == 0) pkv::set_error(p.err, KV_DERR_DST_TABLE);
+                continue;
+            }
+            const int32_t s0 = p.src_req_offsets[r];
+            j0 = (int32_t)((run.stage_block - s0) * (int64_t)p.div_bs.d);
+            const int32_t d0 = p.dst_req_offsets[r];
+            dn = p.dst_req_offsets[r + 1] - d0;
+            dl = p.dst_ids + d0;
+        } else {
+            blk = PACK ? run.src_block : run.dst_block;
+            if (blk < 0 || blk + run.n_blocks > p.num_blocks) {
+                if (first_piece && lane == 0) pkv::set_error(p.err, KV_DERR_BLOCK);
+                continue;
+            }
+        }
+
+        uint8_t *const cache_t = reinterpret_cast<uint8_t *>(p.base[t]);
+        uint8_t *const stage_item = p.stage + (int64_t)(p.tensor_begin + t) * p.stage_tensor_bytes +
+                                    run.stage_block * p.stage_block_bytes;
+
+        for (uint32_t c0 = (uint32_t)c_begin + lane; c0 < c_end; c0 += 32 * kUnroll) {
+            uint4 v[kUnroll];
+            uint8_t *dst[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; u++) {
+                dst[u] = nullptr;
+                const uint32_t c = c0 + 32u * u;
+                if (c >= c_end) continue;
+                uint8_t *cache_addr;
+                if (MODE == MERGED) {
+                    cache_addr = cache_t + blk * p.block_stride + (int64_t)c * 16;
+                } else if (MODE == BLOCKS) {
+                    const uint32_t m = pkv::fdiv(c, p.div_cpb);
+                    const uint32_t w = c - m * p.div_cpb.d;
+                    cache_addr = cache_t + (blk + m) * p.block_stride + (int64_t)w * 16;
+                } else {
+                    const uint32_t row = pkv::fdiv(c, p.div_cpr);
+                    const uint32_t q = c - row * p.div_cpr.d;
+                    const uint32_t m = pkv::fdiv(row, p.div_rpb);
+                    const uint32_t rr = row - m * p.div_rpb.d;
+                    const uint32_t plane = pkv::fdiv(rr, p.div_bs);
+                    const uint32_t o = rr - plane * p.div_bs.d;
+                    if (MODE == ROWS) {
+                        cache_addr = cache_t + (blk + m) * p.block_stride + (int64_t)plane * p.plane_stride +
+                                     (int64_t)o * p.token_stride + p.row_off + (int64_t)q * 16;
+                    } else {  // REMAP: staged token j of the request -> destination slot
+                        const uint32_t j = (uint32_t)j0 + m * p.div_bs.d + o;
+                        const uint32_t dq = pkv::fdiv(j, p.div_dbs);
+                        if ((int32_t)dq >= dn) {
+                            pkv::set_error(p.err, KV_DERR_DST_TABLE);
+                            continue;
+                        }
+                        const int32_t db = dl[dq];
+                        if (db < 0 || db >= p.num_blocks) {
+                            pkv::set_error(p.err, KV_DERR_BLOCK);
+                            continue;
+                        }
+                        const uint32_t doff = j - dq * p.div_dbs.d;
+                        cache_addr = cache_t + (int64_t)db * p.block_stride + (int64_t)plane * p.plane_stride +
+                                     (int64_t)doff * p.token_stride + p.row_off + (int64_t)q * 16;
+                    }
+                }
+                uint8_t *stage_addr = stage_item + (int64_t)c * 16;
+                if (PACK) {
+                    v[u] = pkv::ld_once(cache_addr);
+                    dst[u] = stage_addr;
+                } else {
+                    v[u] = pkv::ld_once(stage_addr);
+                    dst[u] = cache_addr;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; u++)
+                if (dst[u] != nullptr) pkv::st_stream(dst[u], v[u]);
+        }
+    }
+}
+
+using KernelFn = void (*)(CopyParams);
+
+KernelFn pick(int mode, bool pack)
+{
+    switch (mode * 2 + (pack ? 1 : 0)) {
+    case MERGED * 2 + 1: return copy_runs_kernel<MERGED, true>;
+    case MERGED * 2: return copy_runs_kernel<MERGED, false>;
+    case BLOCKS * 2 + 1: return copy_runs_kernel<BLOCKS, true>;
+    case BLOCKS * 2: return copy_runs_kernel<BLOCKS, false>;
+    case ROWS * 2 + 1: return copy_runs_kernel<ROWS, true>;
+    case ROWS * 2: return copy_runs_kernel<ROWS, false>;
+    default: return copy_runs_kernel<REMAP, false>;
+    }
+}
+
+// Resident CTAs per SM of each kernel variant, per device (computed once).
+int resident_ctas(int device, int mode, bool pack)
+{
+    static std::mutex mu;
+    static int cache[64][4][2];
+    std::lock_guard<std::mutex> lock(mu);
+    int &slot = cache[device & 63][mode][pack ? 1 : 0];
+    if (slot == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(mode, pack), kThreads, 0) != cudaSuccess || n <= 0)
+            n = 1;
+        slot = n;
+    }
+    return slot;
+}
+
+bool block_contiguous(const kv_cache_desc *c, int32_t row_off, int32_t slice)
+{
+    return row_off == 0 && slice == c->row_bytes && c->token_stride == c->row_bytes &&
+           (c->n_planes == 1 || c->plane_stride == (int64_t)c->block_size * c->row_bytes);
+}
+
+int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, bool pack, int32_t row_off,
+           const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity, uint8_t *stage_buf,
+           int32_t max_run_blocks, int32_t dst_block_size, const int32_t *src_req_offsets,
+           const int32_t *dst_req_offsets, const int32_t *dst_ids, int32_t n_reqs, cudaStream_t s)
+{
+    const pkv::DeviceInfo *dev = pkv::current_device();
+    if (dev == nullptr) return KV_ERR_CUDA;
+    const int64_t stage_block_bytes = (int64_t)stage->n_planes * stage->block_size * stage->slice_bytes;
+    const int64_t cpb = stage_block_bytes / 16;
+    if (cpb >= (1ll << 31)) return KV_ERR_UNSUPPORTED;
+
+    CopyParams p{};
+    p.runs = runs;
+    p.n_runs = n_runs;
+    p.run_capacity = run_capacity;
+    p.stage = stage_buf;
+    p.stage_block_bytes = stage_block_bytes;
+    p.stage_tensor_bytes = stage->n_blocks * stage_block_bytes;
+    p.n_stage_blocks = stage->n_blocks;
+    p.num_blocks = cache->num_blocks;
+    p.block_stride = cache->block_stride;
+    p.plane_stride = cache->plane_stride;
+    p.token_stride = cache->token_stride;
+    p.row_off = row_off;
+    p.chunks_per_block = (uint32_t)cpb;
+    p.div_cpr = pkv::make_fastdiv((uint32_t)(stage->slice_bytes / 16));
+    p.div_bs = pkv::make_fastdiv((uint32_t)stage->block_size);
+    p.div_rpb = pkv::make_fastdiv((uint32_t)(stage->n_planes * stage->block_size));
+    p.div_cpb = pkv::make_fastdiv((uint32_t)cpb);
+    p.div_dbs = pkv::make_fastdiv((uint32_t)std::max(1, dst_block_size));
+    p.src_req_offsets = src_req_offsets;
+    p.dst_req_offsets = dst_req_offsets;
+    p.dst_ids = dst_ids;
+    p.n_reqs = n_reqs;
+    p.err = dev->err_word;
+    const int64_t run_chunks = (int64_t)std::max(1, max_run_blocks) * cpb;
+    p.max_pieces = max_run_blocks > 0 ? (int32_t)std::min<int64_t>((run_chunks + kPieceChunks - 1) / kPieceChunks, 1 << 20) : 1;
+
+    const KernelFn fn = pick(mode, pack);
+    const int grid = dev->num_sms * resident_ctas(dev->device, mode, pack);
+    for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
+        const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
+        p.n_tensors = nt;
+        p.tensor_begin = t0;
+        for (int32_t t = 0; t < nt; t++) p.base[t] = cache->base[t0 + t];
+        fn<<<grid, kThreads, 0, s>>>(p);
+        const int st = pkv::cuda_status(cudaGetLastError());
+        if (st != KV_OK) return st;
+    }
+    return KV_OK;
+}
+
+int check_stage(const kv_stage_desc *stage, const void *buf, int64_t stage_bytes)
+{
+    if (stage == nullptr || stage->n_blocks < 0 || stage->n_tensors < 0 || stage->block_size <= 0 ||
+        (stage->n_planes != 1 && stage->n_planes != 2) || stage->slice_bytes <= 0 || stage_bytes < 0)
+        return KV_ERR_INVALID_ARG;
+    if (!pkv::aligned16((int64_t)stage->slice_bytes)) return KV_ERR_ALIGN;
+    const int64_t need = stage->n_blocks * stage->n_tensors * stage->n_planes * (int64_t)stage->block_size *
+                         stage->slice_bytes;
+    if (need > 0 && buf == nullptr) return KV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(buf)) return KV_ERR_ALIGN;
+    if (stage_bytes < need) return KV_ERR_RANGE;
+    return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const kv_stage_desc *stage,
+                      const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
+                      int32_t max_run_blocks, void *stage_buf, int64_t stage_bytes, kv_stream_t stream)
+{
+    int st = pkv::check_cache(src);
+    if (st != KV_OK) return st;
+    st = check_stage(stage, stage_buf, stage_bytes);
+    if (st != KV_OK) return st;
+    if (stage->n_tensors != src->n_tensors || stage->n_planes != src->n_planes ||
+        stage->block_size != src->block_size || run_capacity < 0 || max_run_blocks < 0)
+        return KV_ERR_INVALID_ARG;
+    if (src_slice_off < 0 || src_slice_off + (int64_t)stage->slice_bytes > src->row_bytes) return KV_ERR_RANGE;
+    if (!pkv::aligned16((int64_t)src_slice_off)) return KV_ERR_ALIGN;
+    if (src->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0) return KV_OK;
+    if (runs == nullptr || n_runs == nullptr) return KV_ERR_INVALID_ARG;
+    int mode = ROWS;
+    if (block_contiguous(src, src_slice_off, stage->slice_bytes)) {
+        const int64_t blk_bytes = (int64_t)src->n_planes * src->block_size * src->row_bytes;
+        mode = src->block_stride == blk_bytes ? MERGED : BLOCKS;
+    }
+    return launch(src, stage, mode, true, src_slice_off, runs, n_runs, run_capacity, (uint8_t *)stage_buf,
+                  max_run_blocks, 0, nullptr, nullptr, nullptr, 0, (cudaStream_t)stream);
+}
+
+int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
+                        const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
+                        int32_t max_run_blocks, const void *stage_buf, int64_t stage_bytes,
+                        const int32_t *src_req_offsets, const int32_t *dst_req_offsets,
+                        const int32_t *dst_ids, int32_t n_reqs, kv_stream_t stream)
+{
+    int st = pkv::check_cache(dst);
+    if (st != KV_OK) return st;
+    st = check_stage(stage, stage_buf, stage_bytes);
+    if (st != KV_OK) return st;
+    if (stage->n_tensors != dst->n_tensors || stage->n_planes != dst->n_planes || run_capacity < 0 ||
+        max_run_blocks < 0)
+        return KV_ERR_INVALID_ARG;
+    if (dst_slice_off < 0 || dst_slice_off + (int64_t)stage->slice_bytes > dst->row_bytes) return KV_ERR_RANGE;
+    if (!pkv::aligned16((int64_t)dst_slice_off)) return KV_ERR_ALIGN;
+    const bool remap = dst_ids != nullptr;
+    if (remap && (src_req_offsets == nullptr || dst_req_offsets == nullptr || n_reqs < 0))
+        return KV_ERR_INVALID_ARG;
+    if (!remap && stage->block_size != dst->block_size) return KV_ERR_INVALID_ARG;
+    if (dst->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0) return KV_OK;
+    if (runs == nullptr || n_runs == nullptr) return KV_ERR_INVALID_ARG;
+    int mode = REMAP;
+    if (!remap) {
+        mode = ROWS;
+        if (block_contiguous(dst, dst_slice_off, stage->slice_bytes)) {
+            const int64_t blk_bytes = (int64_t)dst->n_planes * dst->block_size * dst->row_bytes;
+            mode = dst->block_stride == blk_bytes ? MERGED : BLOCKS;
+        }
+    }
+    return launch(dst, stage, mode, false, dst_slice_off, runs, n_runs, run_capacity,
+                  (uint8_t *)const_cast<void *>(stage_buf), max_run_blocks, dst->block_size, src_req_offsets,
+                  dst_req_offsets, dst_ids, n_reqs, (cudaStream_t)stream);
+}
+
+}  // extern "C"

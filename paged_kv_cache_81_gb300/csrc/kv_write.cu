@@ -1,0 +1,178 @@
+// kv_slot_mapping and kv_reshape_and_cache: writing new tokens' K/V into the paged cache.
+//
+// Slot formula: drawing "vllm v1 调度逻辑 和 distributed 分布式原理", label "batch tensor 组装";
+// block = slots 0..15 of K/V rows: label "Paged kv cache"; one block_table serves every
+// layer: label "总的就是 all kv cache".
+#include <algorithm>
+
+#include "kv_common.cuh"
+
+namespace {
+
+using pkv::FastDiv;
+
+__global__ void __launch_bounds__(256) slot_mapping_kernel(const int32_t *__restrict__ table, int32_t n_reqs,
+                                                           int32_t max_blocks, int64_t row_stride,
+                                                           const int32_t *__restrict__ token_req,
+                                                           const int32_t *__restrict__ token_pos, int64_t n_tokens,
+                                                           int32_t block_size, int64_t *__restrict__ slot,
+                                                           int *err)
+{
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_tokens; i += step) {
+        const int32_t req = token_req[i];
+        const int32_t pos = token_pos[i];
+        int64_t s = -1;
+        if (req >= 0 && req < n_reqs && pos >= 0) {
+            const int32_t q = pos / block_size;  // logical block of the position
+            if (q < max_blocks) {
+                const int32_t block = table[(int64_t)req * row_stride + q];
+                if (block >= 0) s = (int64_t)block * block_size + (pos - q * block_size);
+            }
+        }
+        if (s < 0) pkv::set_error(err, KV_DERR_TABLE);
+        slot[i] = s;
+    }
+}
+
+// One launch writes up to kMaxTensorsPerLaunch cache tensors (blockIdx.y = tensor).
+// Work is the flat index over (token, plane, 16-byte chunk of the row); consecutive
+// threads cover consecutive chunks of one row, so every row is read and written as
+// whole coalesced segments.
+struct ReshapeParams {
+    const int64_t *slot;
+    int64_t src_token_stride;
+    int64_t block_stride;
+    int64_t plane_stride;
+    int64_t token_stride;
+    uint32_t total;      // n_tokens * n_planes * chunks_per_row
+    uint32_t slot_limit; // num_blocks * block_size
+    FastDiv div_cpr;     // chunks per row
+    FastDiv div_planes;
+    FastDiv div_bs;
+    int32_t n_planes;
+    int *err;
+    uint64_t dst[pkv::kMaxTensorsPerLaunch];
+    uint64_t src[pkv::kMaxTensorsPerLaunch * 2];
+};
+
+constexpr int kReshapeUnroll = 4;
+
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p)
+{
+    const int t = blockIdx.y;
+    uint8_t *const dst = reinterpret_cast<uint8_t *>(p.dst[t]);
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t base = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; base < p.total;
+         base += stride * kReshapeUnroll) {
+        uint4 v[kReshapeUnroll];
+        uint8_t *d[kReshapeUnroll];
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            d[u] = nullptr;
+            const uint64_t idx = base + (uint64_t)u * stride;
+            if (idx >= p.total) continue;
+            const uint32_t row = pkv::fdiv((uint32_t)idx, p.div_cpr);
+            const uint32_t chunk = (uint32_t)idx - row * p.div_cpr.d;
+            const uint32_t tok = pkv::fdiv(row, p.div_planes);
+            const uint32_t plane = row - tok * p.div_planes.d;
+            const int64_t s = p.slot[tok];
+            if (s < 0) continue;  // padding token
+            if (s >= (int64_t)p.slot_limit) {
+                pkv::set_error(p.err, KV_DERR_SLOT);
+                continue;
+            }
+            const uint32_t block = pkv::fdiv((uint32_t)s, p.div_bs);
+            const uint32_t off = (uint32_t)s - block * p.div_bs.d;
+            d[u] = dst + (int64_t)block * p.block_stride + (int64_t)plane * p.plane_stride +
+                   (int64_t)off * p.token_stride + (int64_t)chunk * 16;
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane]);
+            v[u] = pkv::ld_once(src + (int64_t)tok * p.src_token_stride + (int64_t)chunk * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++)
+            if (d[u] != nullptr) pkv::st_stream(d[u], v[u]);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t max_blocks_per_req,
+                    int64_t bt_row_stride, const int32_t *token_req, const int32_t *token_pos,
+                    int64_t n_tokens, int32_t block_size, int64_t *slot_out, kv_stream_t stream)
+{
+    if (n_tokens < 0 || n_reqs < 0 || max_blocks_per_req < 0 || block_size <= 0 || bt_row_stride < 0)
+        return KV_ERR_INVALID_ARG;
+    if (n_tokens == 0) return KV_OK;
+    if (token_req == nullptr || token_pos == nullptr || slot_out == nullptr ||
+        (n_reqs > 0 && max_blocks_per_req > 0 && block_table == nullptr))
+        return KV_ERR_INVALID_ARG;
+    if (n_reqs > 0 && bt_row_stride < max_blocks_per_req) return KV_ERR_INVALID_ARG;
+    const pkv::DeviceInfo *dev = pkv::current_device();
+    if (dev == nullptr) return KV_ERR_CUDA;
+    const int threads = 256;
+    const int64_t need = (n_tokens + threads - 1) / threads;
+    const int blocks = (int)std::min<int64_t>(need, (int64_t)dev->num_sms * 16);
+    slot_mapping_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(
+        block_table, n_reqs, max_blocks_per_req, bt_row_stride, token_req, token_pos, n_tokens, block_size,
+        slot_out, dev->err_word);
+    return pkv::cuda_status(cudaGetLastError());
+}
+
+int kv_reshape_and_cache(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride,
+                         const int64_t *slot, int64_t n_tokens, kv_stream_t stream)
+{
+    int st = pkv::check_cache(cache);
+    if (st != KV_OK) return st;
+    if (n_tokens < 0 || new_token_stride < 0) return KV_ERR_INVALID_ARG;
+    if (n_tokens == 0 || cache->n_tensors == 0) return KV_OK;
+    if (slot == nullptr || new_kv == nullptr) return KV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(new_token_stride)) return KV_ERR_ALIGN;
+    if (new_token_stride < cache->row_bytes) return KV_ERR_RANGE;
+    for (int64_t k = 0; k < (int64_t)cache->n_tensors * cache->n_planes; k++) {
+        if (new_kv[k] == 0) return KV_ERR_INVALID_ARG;
+        if (new_kv[k] & 15u) return KV_ERR_ALIGN;
+    }
+    const int64_t slot_limit = cache->num_blocks * (int64_t)cache->block_size;
+    const int64_t cpr = cache->row_bytes / 16;
+    const int64_t total = n_tokens * cache->n_planes * cpr;
+    if (slot_limit >= (1ll << 31) || total >= (1ll << 31) || cpr >= (1ll << 31)) return KV_ERR_UNSUPPORTED;
+    const pkv::DeviceInfo *dev = pkv::current_device();
+    if (dev == nullptr) return KV_ERR_CUDA;
+
+    ReshapeParams p{};
+    p.slot = slot;
+    p.src_token_stride = new_token_stride;
+    p.block_stride = cache->block_stride;
+    p.plane_stride = cache->plane_stride;
+    p.token_stride = cache->token_stride;
+    p.total = (uint32_t)total;
+    p.slot_limit = (uint32_t)slot_limit;
+    p.div_cpr = pkv::make_fastdiv((uint32_t)cpr);
+    p.div_planes = pkv::make_fastdiv((uint32_t)cache->n_planes);
+    p.div_bs = pkv::make_fastdiv((uint32_t)cache->block_size);
+    p.n_planes = cache->n_planes;
+    p.err = dev->err_word;
+
+    const int threads = 256;
+    const int64_t per_tensor_ctas = (total + (int64_t)threads * kReshapeUnroll - 1) / ((int64_t)threads * kReshapeUnroll);
+    for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
+        const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
+        for (int32_t t = 0; t < nt; t++) {
+            p.dst[t] = cache->base[t0 + t];
+            for (int32_t pl = 0; pl < cache->n_planes; pl++)
+                p.src[t * cache->n_planes + pl] = new_kv[(int64_t)(t0 + t) * cache->n_planes + pl];
+        }
+        // about four waves of 8 resident CTAs per SM over all tensors of the launch
+        const int64_t cap = std::max<int64_t>(1, ((int64_t)dev->num_sms * 8 * 4 + nt - 1) / nt);
+        const dim3 grid((unsigned)std::min(per_tensor_ctas, cap), (unsigned)nt);
+        reshape_and_cache_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(p);
+        st = pkv::cuda_status(cudaGetLastError());
+        if (st != KV_OK) return st;
+    }
+    return KV_OK;
+}
+
+}  // extern "C"

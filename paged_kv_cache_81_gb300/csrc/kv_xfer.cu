@@ -1,0 +1,379 @@
+// kv_build_xfer_list: flattening per-request block lists into maximal contiguous runs.
+//
+// The sender's xfer_list "per layer x per contiguous group x per req" (page "5. flagcx
+// connector design & dev & test", section 1.2) needs, per request, the runs of
+// consecutive block ids; each run is one (source, destination, length) triple (page
+// "vLLM PD 分离 源码级机制", section 4.2, _send_blocks).  The layer factor is applied by
+// the copy kernels, which walk (tensor x run).
+//
+// Single pass over tiles of 2048 list entries, one CTA per tile, tiles taken in launch
+// order from a counter.  Entry i is a natural run start when it opens its request or
+// breaks id contiguity; the cap adds a start wherever (i - s) % cap == 0 for the
+// natural start s of i's run.  A tile's contribution therefore depends on the
+// natural start open at its left edge, which the look-back carries:
+//   aggregate of [a, b):  first and last natural start in it, and the run starts in
+//                         [first natural start, b) (all decidable inside the range);
+//   prefix at b:          last natural start before b and the number of run starts before b.
+// The cap's starts in a stretch [a, b) with no natural start, continuing a run opened at
+// s < a, are counted in closed form: floor((b-1-s)/cap) - floor((a-1-s)/cap).
+#include <algorithm>
+
+#include "kv_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kItems = 8;
+constexpr int kTile = kThreads * kItems;
+constexpr int kWarps = kThreads / 32;
+constexpr int64_t kHeaderBytes = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s bound on any look-back wait
+
+struct TileRecord {  // 32 bytes per tile in the workspace
+    int32_t flag;    // 0 empty, 1 aggregate published, 2 inclusive prefix published
+    int32_t first_nat;
+    int32_t last_nat;
+    int32_t cnt;
+    int32_t pre_s;
+    int32_t pre_cnt;
+    int32_t pad[2];
+};
+
+struct Agg {
+    int32_t first_nat;  // -1: no natural start in the range
+    int32_t last_nat;
+    int32_t cnt;  // run starts in [first_nat, end)
+};
+
+struct Pre {
+    int32_t s;    // last natural start before the position
+    int32_t cnt;  // run starts before the position
+};
+
+__device__ __forceinline__ int32_t cap_starts(int32_t s, int32_t a, int32_t b, int32_t cap)
+{
+    if (cap <= 0 || b <= a) return 0;
+    return (b - 1 - s) / cap - (a - 1 - s) / cap;
+}
+
+// Prefix at b from the prefix at a and the aggregate of [a, b).
+__device__ __forceinline__ Pre apply(const Agg &g, int32_t a, int32_t b, const Pre &p, int32_t cap)
+{
+    if (g.first_nat < 0) return Pre{p.s, p.cnt + cap_starts(p.s, a, b, cap)};
+    return Pre{g.last_nat, p.cnt + cap_starts(p.s, a, g.first_nat, cap) + g.cnt};
+}
+
+// Aggregate of [a, b) from A over [a, m) and B over [m, b).
+__device__ __forceinline__ Agg combine(const Agg &A, const Agg &B, int32_t m, int32_t b, int32_t cap)
+{
+    if (B.first_nat < 0) {
+        if (A.first_nat < 0) return A;
+        return Agg{A.first_nat, A.last_nat, A.cnt + cap_starts(A.last_nat, m, b, cap)};
+    }
+    if (A.first_nat < 0) return B;
+    return Agg{A.first_nat, B.last_nat, A.cnt + cap_starts(A.last_nat, m, B.first_nat, cap) + B.cnt};
+}
+
+__device__ __forceinline__ int32_t ld_acquire(const int32_t *p)
+{
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int32_t *p, int32_t v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+struct Max {
+    __device__ int32_t operator()(int32_t a, int32_t b) const { return a > b ? a : b; }
+};
+struct Min {
+    __device__ int32_t operator()(int32_t a, int32_t b) const { return a < b ? a : b; }
+};
+struct Sum {
+    __device__ int32_t operator()(int32_t a, int32_t b) const { return a + b; }
+};
+
+// Exclusive block-wide scan of one value per thread; *total gets the reduction.
+template <typename Op>
+__device__ int32_t block_exclusive(int32_t v, int32_t identity, Op op, int32_t *sh, int32_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl = op(incl, y);
+    }
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    int32_t before = identity, all = identity;
+#pragma unroll
+    for (int w = 0; w < kWarps; w++) {
+        const int32_t x = sh[w];
+        if (w < warp) before = op(before, x);
+        all = op(all, x);
+    }
+    __syncthreads();
+    int32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = identity;
+    *total = all;
+    return op(before, excl);
+}
+
+struct XferParams {
+    const int32_t *req_offsets;
+    const int32_t *src;
+    const int32_t *dst;  // may be null
+    kv_xfer_run *runs;
+    int32_t *n_runs;
+    uint32_t *counter;
+    TileRecord *tiles;
+    int *err;
+    int64_t capacity;
+    int32_t n_reqs;
+    int32_t n;
+    int32_t cap;
+};
+
+__global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_constant__ XferParams p)
+{
+    __shared__ int32_t sh_scan[kWarps];
+    __shared__ int32_t sh_tile;
+    __shared__ Pre sh_pre;
+
+    const int tid = threadIdx.x;
+    if (tid == 0) sh_tile = (int32_t)atomicAdd(p.counter, 1u);
+    __syncthreads();
+    const int32_t tile = sh_tile;
+    const int32_t tile_start = tile * kTile;
+    const int32_t tile_end = min(tile_start + kTile, p.n);
+    const int32_t i0 = tile_start + tid * kItems;
+
+    if (tile == 0 && tid == 0 && (p.req_offsets[0] != 0 || p.req_offsets[p.n_reqs] != p.n))
+        pkv::set_error(p.err, KV_DERR_LIST);
+
+    // ---- natural run starts of this thread's entries (and of the entry after them) ----
+    bool nat[kItems + 1];
+    int32_t req[kItems];
+    if (i0 < p.n) {
+        int32_t lo = 0, hi = p.n_reqs - 1;  // last request whose first entry is <= i0
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (p.req_offsets[mid] <= i0) lo = mid;
+            else hi = mid - 1;
+        }
+        int32_t r = lo;
+        int32_t begin = p.req_offsets[r], end = p.req_offsets[r + 1];
+        int32_t prev_s = i0 > 0 ? p.src[i0 - 1] : 0;
+        int32_t prev_d = (i0 > 0 && p.dst) ? p.dst[i0 - 1] : 0;
+#pragma unroll
+        for (int k = 0; k <= kItems; k++) {
+            const int32_t i = i0 + k;
+            if (i >= p.n) {
+                nat[k] = true;  // past the list: closes the last run
+                if (k < kItems) req[k] = r;
+                continue;
+            }
+            while (i >= end && r < p.n_reqs - 1) {
+                r++;
+                begin = end;
+                end = p.req_offsets[r + 1];
+            }
+            const int32_t s = p.src[i];
+            const int32_t d = p.dst ? p.dst[i] : 0;
+            nat[k] = (i == begin) || (s != prev_s + 1) || (p.dst != nullptr && d != prev_d + 1);
+            if (k < kItems) req[k] = r;
+            prev_s = s;
+            prev_d = d;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k <= kItems; k++) nat[k] = true;
+#pragma unroll
+        for (int k = 0; k < kItems; k++) req[k] = 0;
+    }
+
+    // ---- tile aggregate from what is decidable locally ----
+    int32_t my_last = -1, my_first = 0x7fffffff;
+#pragma unroll
+    for (int k = 0; k < kItems; k++) {
+        const int32_t i = i0 + k;
+        if (i < tile_end && nat[k]) {
+            my_last = i;
+            my_first = min(my_first, i);
+        }
+    }
+    int32_t tile_last;
+    const int32_t s_before = block_exclusive(my_last, -1, Max(), sh_scan, &tile_last);
+    int32_t tile_first;
+    block_exclusive(my_first, 0x7fffffff, Min(), sh_scan, &tile_first);
+
+    int32_t sk[kItems];  // natural start of each entry's run; -1 while it lies left of the tile
+    int32_t known = 0;
+    {
+        int32_t s = s_before;
+#pragma unroll
+        for (int k = 0; k < kItems; k++) {
+            const int32_t i = i0 + k;
+            if (i < tile_end && nat[k]) s = i;
+            sk[k] = s;
+            if (i < tile_end && s >= 0 && (nat[k] || (p.cap > 0 && (i - s) % p.cap == 0))) known++;
+        }
+    }
+    int32_t tile_cnt;
+    block_exclusive(known, 0, Sum(), sh_scan, &tile_cnt);
+
+    // ---- publish, look back, publish the inclusive prefix ----
+    if (tid == 0) {
+        const Agg agg{tile_first == 0x7fffffff ? -1 : tile_first, tile_last, tile_cnt};
+        TileRecord *rec = p.tiles + tile;
+        Pre excl{-1, 0};
+        if (tile > 0) {
+            rec->first_nat = agg.first_nat;
+            rec->last_nat = agg.last_nat;
+            rec->cnt = agg.cnt;
+            st_release(&rec->flag, 1);
+            Agg suffix{-1, -1, 0};  // aggregate of [(j + 1) * kTile, tile_start)
+            int32_t j = tile - 1;
+            const unsigned long long t_begin = global_ns();
+            unsigned ns = 32;
+            while (true) {
+                const TileRecord *pr = p.tiles + j;
+                int32_t f = ld_acquire(&pr->flag);
+                if (f == 0) {
+                    if (global_ns() - t_begin > kWaitLimitNs) {
+                        pkv::set_error(p.err, KV_DERR_TIMEOUT);
+                        break;  // give up: prefix left at {-1, 0}
+                    }
+                    __nanosleep(ns);
+                    ns = min(ns * 2u, 1024u);
+                    continue;
+                }
+                const int32_t m = (j + 1) * kTile;
+                if (f == 2) {
+                    const Pre pj{__ldcg(&pr->pre_s), __ldcg(&pr->pre_cnt)};
+                    excl = apply(suffix, m, tile_start, pj, p.cap);
+                    break;
+                }
+                const Agg aj{__ldcg(&pr->first_nat), __ldcg(&pr->last_nat), __ldcg(&pr->cnt)};
+                suffix = combine(aj, suffix, m, tile_start, p.cap);
+                j--;
+            }
+        }
+        const Pre incl = apply(agg, tile_start, tile_end, excl, p.cap);
+        rec->pre_s = incl.s;
+        rec->pre_cnt = incl.cnt;
+        st_release(&rec->flag, 2);
+        sh_pre = excl;
+        if (tile_end == p.n) {
+            *p.n_runs = incl.cnt;
+            if ((int64_t)incl.cnt > p.capacity) pkv::set_error(p.err, KV_DERR_CAPACITY);
+        }
+    }
+    __syncthreads();
+    const Pre excl = sh_pre;
+
+    // ---- resolve every entry, number the runs, write each run at its last entry ----
+    bool start[kItems];
+    int32_t mine = 0;
+#pragma unroll
+    for (int k = 0; k < kItems; k++) {
+        const int32_t i = i0 + k;
+        if (sk[k] < 0) sk[k] = excl.s;
+        start[k] = i < tile_end && (nat[k] || (p.cap > 0 && (i - sk[k]) % p.cap == 0));
+        mine += start[k] ? 1 : 0;
+    }
+    int32_t unused;
+    const int32_t before = block_exclusive(mine, 0, Sum(), sh_scan, &unused);
+    int32_t run = excl.cnt + before - 1;  // index of the run holding the current entry
+#pragma unroll
+    for (int k = 0; k < kItems; k++) {
+        const int32_t i = i0 + k;
+        if (i >= tile_end) break;
+        if (start[k]) run++;
+        const bool next_starts = nat[k + 1] || (p.cap > 0 && (i + 1 - sk[k]) % p.cap == 0);
+        if (!next_starts) continue;
+        const int32_t first = p.cap > 0 ? sk[k] + ((i - sk[k]) / p.cap) * p.cap : sk[k];
+        if (first < 0 || first > i) {  // only after a look-back timeout
+            pkv::set_error(p.err, KV_DERR_TIMEOUT);
+            continue;
+        }
+        if ((int64_t)run >= p.capacity || run < 0) {
+            pkv::set_error(p.err, KV_DERR_CAPACITY);
+            continue;
+        }
+        kv_xfer_run out;
+        out.req = req[k];
+        out.src_block = p.src[first];
+        out.dst_block = p.dst ? p.dst[first] : -1;
+        out.n_blocks = i - first + 1;
+        out.stage_block = first;
+        p.runs[run] = out;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_xfer_workspace_bytes(int64_t n_blocks, int64_t *bytes_out)
+{
+    if (bytes_out == nullptr || n_blocks < 0) return KV_ERR_INVALID_ARG;
+    const int64_t tiles = std::max<int64_t>(1, (n_blocks + kTile - 1) / kTile);
+    *bytes_out = kHeaderBytes + tiles * (int64_t)sizeof(TileRecord);
+    return KV_OK;
+}
+
+int kv_build_xfer_list(const int32_t *req_offsets, int32_t n_reqs, const int32_t *src_ids,
+                       const int32_t *dst_ids, int64_t n_blocks, int32_t max_run_blocks,
+                       kv_xfer_run *runs, int64_t run_capacity, int32_t *n_runs,
+                       void *workspace, int64_t workspace_bytes, kv_stream_t stream)
+{
+    if (n_reqs < 0 || n_blocks < 0 || max_run_blocks < 0 || run_capacity < 0 || n_runs == nullptr ||
+        req_offsets == nullptr)
+        return KV_ERR_INVALID_ARG;
+    if (n_blocks >= (1ll << 31) - kTile) return KV_ERR_UNSUPPORTED;
+    if (n_blocks > 0 && (n_reqs == 0 || src_ids == nullptr || (run_capacity > 0 && runs == nullptr)))
+        return KV_ERR_INVALID_ARG;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (n_blocks == 0) return pkv::cuda_status(cudaMemsetAsync(n_runs, 0, sizeof(int32_t), s));
+    int64_t need = 0;
+    kv_xfer_workspace_bytes(n_blocks, &need);
+    if (workspace == nullptr) return KV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(workspace)) return KV_ERR_ALIGN;
+    if (workspace_bytes < need) return KV_ERR_RANGE;
+    if (((uintptr_t)runs & 7u) != 0) return KV_ERR_ALIGN;
+    const pkv::DeviceInfo *dev = pkv::current_device();
+    if (dev == nullptr) return KV_ERR_CUDA;
+
+    int st = pkv::cuda_status(cudaMemsetAsync(workspace, 0, (size_t)need, s));
+    if (st != KV_OK) return st;
+    XferParams p{};
+    p.req_offsets = req_offsets;
+    p.src = src_ids;
+    p.dst = dst_ids;
+    p.runs = runs;
+    p.n_runs = n_runs;
+    p.counter = reinterpret_cast<uint32_t *>(workspace);
+    p.tiles = reinterpret_cast<TileRecord *>(reinterpret_cast<uint8_t *>(workspace) + kHeaderBytes);
+    p.err = dev->err_word;
+    p.capacity = run_capacity;
+    p.n_reqs = n_reqs;
+    p.n = (int32_t)n_blocks;
+    p.cap = max_run_blocks;
+    const int tiles = (int)((n_blocks + kTile - 1) / kTile);
+    build_xfer_kernel<<<tiles, kThreads, 0, s>>>(p);
+    return pkv::cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,301 @@
+"""ctypes binding of libpagedkv.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch CUDA
+tensors, passes their data pointers and the current CUDA stream, and raises
+``KvError`` on a non-zero status.  No step of the data path runs in Python or on the
+CPU: when the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+KV_OK, KV_ERR_INVALID_ARG, KV_ERR_ALIGN, KV_ERR_RANGE, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_ERR_UNSUPPORTED = range(7)
+KV_DERR_TABLE, KV_DERR_SLOT, KV_DERR_BLOCK, KV_DERR_LIST = 0x01, 0x02, 0x04, 0x08
+KV_DERR_CAPACITY, KV_DERR_STAGE, KV_DERR_DST_TABLE, KV_DERR_TIMEOUT = 0x10, 0x20, 0x40, 0x80
+
+RUN_WORDS = 6  # a kv_xfer_run is 24 bytes: six int32 words (the last two hold the int64 stage_block)
+EXPORTS = ("kv_version", "kv_status_string", "kv_last_cuda_error", "kv_slot_mapping", "kv_reshape_and_cache",
+           "kv_xfer_workspace_bytes", "kv_build_xfer_list", "kv_pack_blocks", "kv_unpack_blocks",
+           "kv_get_last_error")
+
+
+class KvError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn} failed: {_status_name(status)}{(' ' + detail) if detail else ''}")
+
+
+class KvCacheDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_tensors", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("n_planes", ctypes.c_int32),
+        ("row_bytes", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64),
+        ("block_stride", ctypes.c_int64),
+        ("plane_stride", ctypes.c_int64),
+        ("token_stride", ctypes.c_int64),
+        ("base", ctypes.POINTER(ctypes.c_uint64)),
+    ]
+
+
+class KvStageDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_blocks", ctypes.c_int64),
+        ("n_tensors", ctypes.c_int32),
+        ("n_planes", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("slice_bytes", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load and bind libpagedkv.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        D = ctypes.POINTER(KvCacheDesc)
+        S = ctypes.POINTER(KvStageDesc)
+        sig = {
+            "kv_version": ([], ctypes.c_char_p),
+            "kv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "kv_last_cuda_error": ([], ctypes.c_int),
+            "kv_slot_mapping": ([P, i32, i32, i64, P, P, i64, i32, P, P], ctypes.c_int),
+            "kv_reshape_and_cache": ([D, P, i64, P, i64, P], ctypes.c_int),
+            "kv_xfer_workspace_bytes": ([i64, ctypes.POINTER(i64)], ctypes.c_int),
+            "kv_build_xfer_list": ([P, i32, P, P, i64, i32, P, i64, P, P, i64, P], ctypes.c_int),
+            "kv_pack_blocks": ([D, i32, S, P, P, i64, i32, P, i64, P], ctypes.c_int),
+            "kv_unpack_blocks": ([D, i32, S, P, P, i64, i32, P, i64, P, P, P, i32, P], ctypes.c_int),
+            "kv_get_last_error": ([ctypes.POINTER(i32), i32, P], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes, f.restype = args, res
+        _lib = lib
+        return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load().kv_status_string(status).decode()
+    except Exception:  # the library may be what is missing
+        return f"status {status}"
+
+
+def _check(fn: str, status: int):
+    if status != KV_OK:
+        detail = f"(cuda error {load().kv_last_cuda_error()})" if status == KV_ERR_CUDA else ""
+        raise KvError(fn, status, detail)
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libpagedkv takes CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _i32(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def version() -> str:
+    return load().kv_version().decode()
+
+
+# ---------------------------------------------------------------------------
+# cache geometry
+# ---------------------------------------------------------------------------
+@dataclass
+class PagedCache:
+    """A paged cache: equal-shaped device tensors plus their byte geometry (kv_cache_desc)."""
+
+    tensors: list
+    num_blocks: int
+    block_size: int
+    n_planes: int
+    row_bytes: int
+    block_stride: int
+    plane_stride: int
+    token_stride: int
+
+    @classmethod
+    def from_tensors(cls, tensors: Sequence[torch.Tensor], layout: str) -> "PagedCache":
+        """layout: "separate" / "mla" ([num_blocks, bs, ...row]), "blocks_first"
+        ([num_blocks, 2, bs, ...row]) or "kv_first" ([2, num_blocks, bs, ...row])."""
+        tensors = list(tensors)
+        t = tensors[0]
+        e = t.element_size()
+        st = [s * e for s in t.stride()]
+        if layout in ("separate", "mla"):
+            nb, bs, planes = t.shape[0], t.shape[1], 1
+            block, plane, token, rest = st[0], st[0], st[1], t.shape[2:]
+        elif layout == "blocks_first":
+            nb, bs, planes = t.shape[0], t.shape[2], 2
+            block, plane, token, rest = st[0], st[1], st[2], t.shape[3:]
+            assert t.shape[1] == 2
+        elif layout == "kv_first":
+            nb, bs, planes = t.shape[1], t.shape[2], 2
+            block, plane, token, rest = st[1], st[0], st[2], t.shape[3:]
+            assert t.shape[0] == 2
+        else:
+            raise ValueError(layout)
+        row = e
+        for d in rest:
+            row *= d
+        for x in tensors:
+            if x.shape != t.shape or x.stride() != t.stride() or x.dtype != t.dtype or not x.is_cuda:
+                raise ValueError("cache tensors must share shape, strides and dtype and live on the GPU")
+        return cls(tensors, int(nb), int(bs), planes, int(row), int(block), int(plane), int(token))
+
+    def desc(self) -> KvCacheDesc:
+        n = len(self.tensors)
+        self._bases = (ctypes.c_uint64 * max(1, n))(*[x.data_ptr() for x in self.tensors])
+        return KvCacheDesc(n, self.block_size, self.n_planes, self.row_bytes, self.num_blocks, self.block_stride,
+                           self.plane_stride, self.token_stride,
+                           ctypes.cast(self._bases, ctypes.POINTER(ctypes.c_uint64)))
+
+
+def stage_desc(n_blocks: int, n_tensors: int, n_planes: int, block_size: int, slice_bytes: int) -> KvStageDesc:
+    return KvStageDesc(int(n_blocks), int(n_tensors), int(n_planes), int(block_size), int(slice_bytes))
+
+
+def stage_nbytes(sd: KvStageDesc) -> int:
+    return sd.n_blocks * sd.n_tensors * sd.n_planes * sd.block_size * sd.slice_bytes
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def kv_slot_mapping(block_table: torch.Tensor, token_req: torch.Tensor, token_pos: torch.Tensor, block_size: int,
+                    slot_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    _i32(token_req, "token_req"), _i32(token_pos, "token_pos")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be a row-major int32 [n_reqs, max_blocks] CUDA tensor")
+    n = token_req.shape[0]
+    if slot_out is None:
+        slot_out = torch.empty(n, dtype=torch.int64, device=token_req.device)
+    _check("kv_slot_mapping", load().kv_slot_mapping(
+        _ptr(block_table), block_table.shape[0], block_table.shape[1], block_table.stride(0), _ptr(token_req),
+        _ptr(token_pos), n, int(block_size), _ptr(slot_out), _stream(stream)))
+    return slot_out
+
+
+def kv_reshape_and_cache(cache: PagedCache, new_kv: Sequence[torch.Tensor], slot: torch.Tensor, stream=None):
+    """new_kv: n_tensors * n_planes tensors [T, ...row] (tensor-major, plane-minor), equal strides."""
+    if slot.dtype != torch.int64:
+        raise ValueError("slot must be int64")
+    new_kv = list(new_kv)
+    stride = new_kv[0].stride(0) * new_kv[0].element_size() if new_kv else cache.row_bytes
+    ptrs = (ctypes.c_uint64 * max(1, len(new_kv)))(*[x.data_ptr() for x in new_kv])
+    d = cache.desc()
+    _check("kv_reshape_and_cache", load().kv_reshape_and_cache(
+        ctypes.byref(d), ctypes.cast(ptrs, ctypes.c_void_p), stride, _ptr(slot), slot.shape[0], _stream(stream)))
+
+
+def kv_xfer_workspace_bytes(n_blocks: int) -> int:
+    out = ctypes.c_int64(0)
+    _check("kv_xfer_workspace_bytes", load().kv_xfer_workspace_bytes(int(n_blocks), ctypes.byref(out)))
+    return out.value
+
+
+class XferList:
+    """Device output of kv_build_xfer_list: run records [capacity, 6] int32 and the run count."""
+
+    def __init__(self, capacity: int, device, max_run_blocks: int):
+        self.capacity = int(capacity)
+        self.max_run_blocks = int(max_run_blocks)
+        self.runs = torch.empty((max(1, self.capacity), RUN_WORDS), dtype=torch.int32, device=device)
+        self.n_runs = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def host(self) -> dict:
+        """Copy the runs to the host as numpy columns (synchronises)."""
+        n = min(int(self.n_runs.item()), self.capacity)
+        r = self.runs[:n].cpu()
+        return dict(req=r[:, 0].numpy(), src_block=r[:, 1].numpy(), dst_block=r[:, 2].numpy(),
+                    n_blocks=r[:, 3].numpy(), stage_block=r[:, 4:6].contiguous().view(torch.int64)[:, 0].numpy(),
+                    count=int(self.n_runs.item()))
+
+
+def kv_build_xfer_list(req_offsets: torch.Tensor, src_ids: torch.Tensor, dst_ids: Optional[torch.Tensor] = None,
+                       max_run_blocks: int = 0, out: Optional[XferList] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> XferList:
+    _i32(req_offsets, "req_offsets"), _i32(src_ids, "src_ids")
+    if dst_ids is not None:
+        _i32(dst_ids, "dst_ids")
+    n = src_ids.shape[0]
+    if out is None:
+        out = XferList(n, src_ids.device, max_run_blocks)
+    ws_bytes = kv_xfer_workspace_bytes(n)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=src_ids.device)
+    _check("kv_build_xfer_list", load().kv_build_xfer_list(
+        _ptr(req_offsets), req_offsets.shape[0] - 1, _ptr(src_ids), _ptr(dst_ids), n, int(max_run_blocks),
+        _ptr(out.runs), out.capacity, _ptr(out.n_runs), _ptr(workspace), workspace.numel(), _stream(stream)))
+    out.max_run_blocks = int(max_run_blocks)
+    return out
+
+
+def kv_pack_blocks(cache: PagedCache, xfer: XferList, n_blocks: int, stage: Optional[torch.Tensor] = None,
+                   slice_off: int = 0, slice_bytes: Optional[int] = None, stream=None) -> torch.Tensor:
+    sb = cache.row_bytes if slice_bytes is None else int(slice_bytes)
+    sd = stage_desc(n_blocks, len(cache.tensors), cache.n_planes, cache.block_size, sb)
+    if stage is None:
+        stage = torch.empty(stage_nbytes(sd), dtype=torch.uint8, device=xfer.runs.device)
+    d = cache.desc()
+    _check("kv_pack_blocks", load().kv_pack_blocks(
+        ctypes.byref(d), int(slice_off), ctypes.byref(sd), _ptr(xfer.runs), _ptr(xfer.n_runs), xfer.capacity,
+        xfer.max_run_blocks, _ptr(stage), stage.numel() * stage.element_size(), _stream(stream)))
+    return stage
+
+
+def kv_unpack_blocks(cache: PagedCache, stage: torch.Tensor, xfer: XferList, n_blocks: int, src_block_size: int,
+                     slice_bytes: Optional[int] = None, dst_slice_off: int = 0,
+                     src_req_offsets: Optional[torch.Tensor] = None, dst_req_offsets: Optional[torch.Tensor] = None,
+                     dst_ids: Optional[torch.Tensor] = None, stream=None):
+    """Whole-block mode when dst_ids is None (runs carry destination ids), remap mode otherwise."""
+    sb = cache.row_bytes if slice_bytes is None else int(slice_bytes)
+    sd = stage_desc(n_blocks, len(cache.tensors), cache.n_planes, src_block_size, sb)
+    n_reqs = 0 if dst_req_offsets is None else dst_req_offsets.shape[0] - 1
+    d = cache.desc()
+    _check("kv_unpack_blocks", load().kv_unpack_blocks(
+        ctypes.byref(d), int(dst_slice_off), ctypes.byref(sd), _ptr(xfer.runs), _ptr(xfer.n_runs), xfer.capacity,
+        xfer.max_run_blocks, _ptr(stage), stage.numel() * stage.element_size(), _ptr(src_req_offsets),
+        _ptr(dst_req_offsets), _ptr(dst_ids), n_reqs, _stream(stream)))
+
+
+def kv_get_last_error(clear: bool = True, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check("kv_get_last_error", load().kv_get_last_error(ctypes.byref(out), 1 if clear else 0, _stream(stream)))
+    return out.value
+
+
+def default_max_run_blocks(stage_block_bytes: int, target_bytes: int = 64 * 1024) -> int:
+    """A run cap that keeps one run at or under target_bytes per tensor (at least one block)."""
+    return max(1, int(target_bytes) // max(1, int(stage_block_bytes)))

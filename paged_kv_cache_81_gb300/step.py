@@ -1,0 +1,127 @@
+"""One pass of the paged KV-cache hot path over one batch, through the C ABI.
+
+A step runs, on one CUDA stream:
+  1. kv_slot_mapping        new tokens' slots from the shared block table (when the batch has new tokens)
+  2. kv_reshape_and_cache   their K/V rows into every layer's paged tensor
+  3. kv_build_xfer_list     the send side's per-request block lists -> contiguous runs
+  4. kv_pack_blocks         those runs of every tensor -> the staging buffer
+  5. kv_unpack_blocks       the staging buffer -> the receiver's cache (whole blocks, or
+                            token-granular onto another block size / head slice)
+This module only allocates the step's buffers and orders the calls; every step of the
+data path runs in libpagedkv.so.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import pagedkv as K
+from .workloads import Case, Workload
+
+
+@dataclass
+class StepBytes:
+    """Algorithmic bytes of each call of one step (payload read + written, plus index arrays)."""
+
+    slot_mapping: int
+    reshape_and_cache: int
+    build_xfer_list: int
+    pack: int
+    unpack: int
+
+    @property
+    def total(self) -> int:
+        return self.slot_mapping + self.reshape_and_cache + self.build_xfer_list + self.pack + self.unpack
+
+
+class TransferStep:
+    def __init__(self, wl: Workload, case: Case, src_tensors, dst_tensors=None, new_kv=None,
+                 max_run_blocks: Optional[int] = None, device="cuda"):
+        self.wl, self.case = wl, case
+        self.device = torch.device(device)
+        self.src = K.PagedCache.from_tensors(src_tensors, wl.src.layout)
+        self.dst = K.PagedCache.from_tensors(dst_tensors, wl.dst.layout) if dst_tensors is not None else None
+        self.new_kv = list(new_kv) if new_kv is not None else []
+        dev = self.device
+
+        def t(a):
+            return torch.from_numpy(a).to(dev)
+
+        self.req_offsets = t(case.req_offsets)
+        self.src_ids = t(case.src_ids)
+        self.equal = wl.equal_geometry
+        self.dst_req_offsets = t(case.dst_req_offsets)
+        self.dst_ids = t(case.dst_ids)
+        self.n_tokens = case.n_tokens
+        if self.n_tokens:
+            self.block_table = t(case.block_table)
+            self.token_req = t(case.token_req)
+            self.token_pos = t(case.token_pos)
+            self.slot = torch.empty(self.n_tokens, dtype=torch.int64, device=dev)
+        self.slice_off = wl.slice_off
+        self.slice_bytes = wl.moved_slice
+        stage_block = wl.src.n_planes * wl.src.block_size * self.slice_bytes
+        self.max_run_blocks = K.default_max_run_blocks(stage_block) if max_run_blocks is None else max_run_blocks
+        n = case.n_blocks
+        self.xfer = K.XferList(n, dev, self.max_run_blocks)
+        self.workspace = torch.empty(K.kv_xfer_workspace_bytes(n), dtype=torch.uint8, device=dev)
+        sd = K.stage_desc(n, len(self.src.tensors), wl.src.n_planes, wl.src.block_size, self.slice_bytes)
+        self.stage = torch.empty(max(16, K.stage_nbytes(sd)), dtype=torch.uint8, device=dev)
+
+    # -- the five calls ---------------------------------------------------------
+    def write_tokens(self, stream=None):
+        if not self.n_tokens:
+            return
+        K.kv_slot_mapping(self.block_table, self.token_req, self.token_pos, self.src.block_size, self.slot, stream)
+        K.kv_reshape_and_cache(self.src, self.new_kv, self.slot, stream)
+
+    def build(self, stream=None):
+        dst = self.dst_ids if (self.equal and self.dst is not None) else None
+        K.kv_build_xfer_list(self.req_offsets, self.src_ids, dst, self.max_run_blocks, self.xfer, self.workspace,
+                             stream)
+
+    def pack(self, stream=None):
+        K.kv_pack_blocks(self.src, self.xfer, self.case.n_blocks, self.stage, self.slice_off, self.slice_bytes,
+                         stream)
+
+    def unpack(self, stream=None):
+        if self.dst is None:
+            return
+        if self.equal:
+            K.kv_unpack_blocks(self.dst, self.stage, self.xfer, self.case.n_blocks, self.wl.src.block_size,
+                               self.slice_bytes, self.wl.dst_slice_off, stream=stream)
+        else:
+            K.kv_unpack_blocks(self.dst, self.stage, self.xfer, self.case.n_blocks, self.wl.src.block_size,
+                               self.slice_bytes, self.wl.dst_slice_off, self.req_offsets, self.dst_req_offsets,
+                               self.dst_ids, stream=stream)
+
+    def run(self, stream=None):
+        self.write_tokens(stream)
+        self.build(stream)
+        self.pack(stream)
+        self.unpack(stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        """Kernels of libpagedkv one run() launches (one launch per 128 tensors for the copies)."""
+        groups = -(-len(self.src.tensors) // 128)
+        n = 1 + groups  # builder + pack
+        if self.n_tokens:
+            n += 1 + groups
+        if self.dst is not None:
+            n += groups
+        return n
+
+    # -- algorithmic bytes ----------------------------------------------------
+    def bytes(self) -> StepBytes:
+        wl, case = self.wl, self.case
+        nt = len(self.src.tensors)
+        payload = nt * case.n_blocks * wl.src.n_planes * wl.src.block_size * self.slice_bytes
+        n_runs_words = 24  # per run record written by the builder / read by a copy kernel
+        T = self.n_tokens
+        slot_b = T * (4 + 4 + 4 + 8) if T else 0  # req, pos, table entry read; slot written
+        reshape_b = (nt * wl.src.n_planes * T * wl.src.row_bytes * 2 + T * 8) if T else 0
+        build_b = case.n_blocks * 4 * (2 if (self.equal and self.dst is not None) else 1)
+        return StepBytes(slot_b, reshape_b, build_b, 2 * payload, 2 * payload if self.dst is not None else 0)

@@ -386,3 +386,35 @@ def fill_random_(t, seed: int):
     g = torch.Generator(device=t.device).manual_seed(int(seed))
     t.view(torch.int32).random_(-2 ** 31, 2 ** 31, generator=g)
     return t
+
+
+# --- device tensors (torch; used by the GPU tests and the benchmark) ---------
+def to_device_bf16(arrays, device):
+    """Host uint16 bf16-pattern arrays -> torch bf16 tensors on `device` (bit-identical)."""
+    import torch
+
+    return [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device) for a in arrays]
+
+
+def device_cache(geom: CacheGeom, n_tensors: int, device, seed: Optional[int] = None):
+    """n_tensors bf16 device tensors of geom's shape, filled with seeded random bits (or left unset)."""
+    import torch
+
+    out = []
+    for t in range(n_tensors):
+        x = torch.empty(geom.tensor_shape(), dtype=torch.bfloat16, device=device)
+        if seed is not None:
+            fill_random_(x, seed * 1000003 + t)
+        out.append(x)
+    return out
+
+
+def new_token_rows(geom: CacheGeom, n_tensors: int, n_tokens: int, device, seed: int):
+    """New K/V rows for n_tokens tokens: n_tensors * n_planes views [T, H, D] of one bf16 buffer."""
+    import torch
+
+    h, d = (1, geom.heads * geom.head_dim) if geom.layout == "mla" else (geom.heads, geom.head_dim)
+    buf = torch.empty((n_tensors * geom.n_planes, n_tokens, h, d), dtype=torch.bfloat16, device=device)
+    if n_tokens:
+        fill_random_(buf, seed)
+    return [buf[k] for k in range(buf.shape[0])]

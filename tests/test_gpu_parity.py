@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit-exact.
+
+Every output is compared element by element: slots, run records, the staging buffer,
+the source cache after reshape_and_cache and the destination cache after unpack.
+Cases: the five presets at reduced sizes (several builder tiles, ragged last
+blocks), the Tiny preset in full, and edge cases (empty lists, capacity overflow,
+out-of-range ids, padding slots, every cache layout and address mode).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_81_gb300 import pagedkv as K
+from paged_kv_cache_81_gb300 import workloads as W
+from tests import gpu_support as G
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_81_gb300 import build
+    build.build()
+    K.load()
+
+
+PRESETS = [W.TINY, W.small(W.MID), W.small(W.PAGE), W.small(W.MLA), W.small(W.ASYM)]
+
+
+@pytest.mark.parametrize("wl", PRESETS, ids=lambda w: w.name)
+def test_preset_parity(wl):
+    case = W.make_case(wl)
+    src, dst, new = G.host_inputs(wl, case, seed=wl.seed + 1000)
+    gpu = G.run_gpu(wl, case, src, dst, new)
+    ora = G.run_oracle(wl, case, src, dst, new, gpu["max_run_blocks"])
+    G.compare(gpu, ora, wl.name)
+
+
+@pytest.mark.parametrize("cap", [0, 1, 3])
+@pytest.mark.parametrize("wl", [W.small(W.MID), W.small(W.ASYM)], ids=lambda w: w.name)
+def test_run_cap_variants(wl, cap):
+    case = W.make_case(wl)
+    src, dst, new = G.host_inputs(wl, case, seed=7)
+    gpu = G.run_gpu(wl, case, src, dst, new, max_run_blocks=cap)
+    ora = G.run_oracle(wl, case, src, dst, new, cap)
+    G.compare(gpu, ora, f"{wl.name} cap {cap}")
+
+
+def _builder_case(n_reqs, lens, rng, frag=(12, 0.6), n_ids=None):
+    n_ids = n_ids or int(sum(lens)) + 7
+    q = W.fragmented_queue(rng, n_ids, *frag)
+    return W.csr(W.pop_lists(q, lens))
+
+
+@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096, 6145, 20000, 100003])
+@pytest.mark.parametrize("cap", [0, 1, 2, 7, 32])
+def test_builder_tiles(n, cap):
+    """Runs across tile boundaries, long runs, empty requests, all cap variants."""
+    rng = np.random.default_rng(n * 31 + cap)
+    lens = []
+    left = n
+    while left > 0:
+        k = int(min(left, rng.integers(0, 3000)))
+        lens.append(k)
+        left -= k
+    lens.insert(len(lens) // 2, 0)  # an empty request in the middle
+    off, ids = _builder_case(len(lens), lens, rng, frag=(int(rng.integers(1, 64)), 0.8))
+    dq = W.fragmented_queue(rng, n + 9, 40, 0.9)
+    dids = dq[:n].astype(np.int32)
+    for with_dst in (False, True):
+        d = torch.from_numpy(dids).cuda() if with_dst else None
+        x = K.kv_build_xfer_list(torch.from_numpy(off).cuda(), torch.from_numpy(ids).cuda(), d, cap)
+        torch.cuda.synchronize()
+        got = x.host()
+        want = oracle.build_xfer_list(off, ids, dids if with_dst else None, cap)
+        assert got["count"] == want["req"].shape[0]
+        for key in want:
+            np.testing.assert_array_equal(got[key], want[key], err_msg=f"{key} n={n} cap={cap} dst={with_dst}")
+    assert K.kv_get_last_error() == 0
+
+
+def test_builder_empty_and_capacity():
+    off = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ids = torch.zeros(0, dtype=torch.int32, device="cuda")
+    x = K.kv_build_xfer_list(off, ids)
+    torch.cuda.synchronize()
+    assert x.host()["count"] == 0 and K.kv_get_last_error() == 0
+    # more runs than capacity: the count is exact, the first `capacity` runs are written, the error bit is set
+    o, s = W.csr([[5, 9, 11, 12, 3], [4]])
+    want = oracle.build_xfer_list(o, s)
+    out = K.XferList(2, "cuda", 0)
+    K.kv_build_xfer_list(torch.from_numpy(o).cuda(), torch.from_numpy(s).cuda(), out=out)
+    torch.cuda.synchronize()
+    got = out.host()
+    assert got["count"] == 5
+    np.testing.assert_array_equal(got["src_block"], want["src_block"][:2])
+    assert K.kv_get_last_error() & K.KV_DERR_CAPACITY
+
+
+def test_builder_bad_offsets_flagged():
+    o = torch.tensor([0, 3, 5], dtype=torch.int32, device="cuda")  # claims 5 entries, list has 4
+    s = torch.tensor([1, 2, 3, 4], dtype=torch.int32, device="cuda")
+    K.kv_build_xfer_list(o, s)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() & K.KV_DERR_LIST
+
+
+def test_slot_mapping_golden_and_invalid():
+    """The hand-worked golden cases (padded to one table) and invalid tokens -> -1 + error bit."""
+    for case, bs, table, pos, want in H.read_slot_golden():
+        bt = torch.tensor([table], dtype=torch.int32, device="cuda")
+        got = K.kv_slot_mapping(bt, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                                torch.tensor([pos], dtype=torch.int32, device="cuda"), bs)
+        torch.cuda.synchronize()
+        assert int(got.item()) == want, (case, bs, table, pos)
+        err = K.kv_get_last_error()
+        assert bool(err & K.KV_DERR_TABLE) == (want < 0)
+    bt = torch.tensor([[3, 7], [8, 9]], dtype=torch.int32, device="cuda")
+    req = torch.tensor([0, 2, -1, 1], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([1, 0, 0, -3], dtype=torch.int32, device="cuda")
+    got = K.kv_slot_mapping(bt, req, pos, 2).cpu().numpy()
+    np.testing.assert_array_equal(got, [7, -1, -1, -1])
+    assert K.kv_get_last_error() & K.KV_DERR_TABLE
+
+
+def test_slot_mapping_large_random():
+    rng = np.random.default_rng(3)
+    R, M, bs, nb = 300, 70, 16, 50000
+    table = rng.integers(0, nb, size=(R, M)).astype(np.int32)
+    T = 100000
+    req = rng.integers(0, R, T).astype(np.int32)
+    pos = rng.integers(0, M * bs, T).astype(np.int32)
+    got = K.kv_slot_mapping(torch.from_numpy(table).cuda(), torch.from_numpy(req).cuda(),
+                            torch.from_numpy(pos).cuda(), bs).cpu().numpy()
+    want, bad = oracle.slot_mapping(table, req, pos, bs)
+    assert bad == 0
+    np.testing.assert_array_equal(got, want)
+    assert K.kv_get_last_error() == 0
+
+
+def _layout_case(layout, nb=40, bs=16, heads=4, hd=32, seed=0):
+    g = W.CacheGeom(layout, nb, bs, heads, hd) if layout != "mla" else W.CacheGeom("mla", nb, bs, 1, heads * hd)
+    rng = np.random.default_rng(seed)
+    host = W.host_cache_tensors(g, 3, rng)
+    perm = rng.permutation(nb)
+    lists = [perm[0:5], perm[5:5], np.array([perm[5], perm[5] + 1 if perm[5] + 1 < nb else perm[6]]), perm[7:20]]
+    off, ids = W.csr(lists)
+    return g, host, off, ids
+
+
+@pytest.mark.parametrize("layout", ["separate", "blocks_first", "kv_first", "mla"])
+@pytest.mark.parametrize("sl", [None, (32, 64)])
+def test_pack_layouts(layout, sl):
+    """Every layout and address mode: MERGED (dense), ROWS (kv-first planes, head slice)."""
+    g, host, off, ids = _layout_case(layout, seed=W.LAYOUTS.index(layout) + 17)
+    s_off, s_len = (0, g.row_bytes) if sl is None else sl
+    dev = W.to_device_bf16(host, "cuda")
+    cache = K.PagedCache.from_tensors(dev, layout)
+    x = K.kv_build_xfer_list(torch.from_numpy(off).cuda(), torch.from_numpy(ids).cuda(), None, 4)
+    stage = K.kv_pack_blocks(cache, x, ids.shape[0], slice_off=s_off, slice_bytes=s_len)
+    want = oracle.pack(H.ora_cache(g, host), off, ids, s_off, s_len)
+    np.testing.assert_array_equal(stage.cpu().numpy(), want)
+    assert K.kv_get_last_error() == 0
+
+
+def test_pack_unpack_strided_blocks():
+    """BLOCKS mode: each block contiguous, blocks further apart than their size (a padded view)."""
+    nb, bs, heads, hd = 30, 8, 2, 16
+    rng = np.random.default_rng(5)
+    full = [torch.from_numpy(rng.integers(-2 ** 15, 2 ** 15, size=(nb, 2 * bs, heads, hd), dtype=np.int16)).cuda()
+            for _ in range(2)]
+    views = [f.view(torch.bfloat16)[:, :bs] for f in full]  # block_stride = 2 * bs * row
+    cache = K.PagedCache.from_tensors(views, "separate")
+    assert cache.block_stride == 2 * bs * heads * hd * 2
+    off, ids = W.csr([[3, 4, 5, 9], [0, 1]])
+    x = K.kv_build_xfer_list(torch.from_numpy(off).cuda(), torch.from_numpy(ids).cuda(), None, 3)
+    stage = K.kv_pack_blocks(cache, x, ids.shape[0])
+    host = [v.cpu().view(torch.int16).numpy() for v in views]
+    want = np.concatenate([np.concatenate([h[i].reshape(-1).view(np.uint8) for i in ids]) for h in host])
+    np.testing.assert_array_equal(stage.cpu().numpy(), want)
+    # unpack back into other blocks of the padded views: the padding rows must stay untouched
+    before = [f.clone() for f in full]
+    d_off, d_ids = W.csr([[10, 11, 12, 20], [21, 22]])
+    x2 = K.kv_build_xfer_list(torch.from_numpy(off).cuda(), torch.from_numpy(ids).cuda(),
+                              torch.from_numpy(d_ids).cuda(), 3)
+    K.kv_unpack_blocks(cache, stage, x2, ids.shape[0], bs)
+    torch.cuda.synchronize()
+    for f, b, h in zip(full, before, host):
+        fh, bh = f.cpu().numpy(), b.cpu().numpy()
+        np.testing.assert_array_equal(fh[:, bs:], bh[:, bs:])  # padding untouched
+        for s_, d_ in zip(ids, d_ids):
+            np.testing.assert_array_equal(fh[d_, :bs], h[s_])
+    assert K.kv_get_last_error() == 0
+
+
+@pytest.mark.parametrize("dbs,dheads,d_off", [(64, 4, 0), (24, 4, 0), (16, 8, 512)])
+def test_unpack_remap_variants(dbs, dheads, d_off):
+    """Token-granular unpack: 16 -> 64, the non-multiple 16 -> 24, and a slice landing mid-row."""
+    sg = W.CacheGeom("separate", 256, 16, 8, 64)  # 1 KiB rows
+    dg = W.CacheGeom("separate", 200, dbs, dheads, 64)
+    rng = np.random.default_rng(dbs)
+    src = W.host_cache_tensors(sg, 2, rng)
+    dst = W.host_cache_tensors(dg, 2, rng)
+    lens = [37, 1, 130, 64]
+    s_lists = W.pop_lists(rng.permutation(256).astype(np.int32), [-(-l // 16) for l in lens])
+    need = [-(-len(l) * 16 // dbs) for l in s_lists]
+    d_lists = W.pop_lists(rng.permutation(200).astype(np.int32), need)
+    off, ids = W.csr(s_lists)
+    doff, dids = W.csr(d_lists)
+    s_off, s_len = 256, 512  # heads 2..5 of the source row
+    dd = W.to_device_bf16(dst, "cuda")
+    scache = K.PagedCache.from_tensors(W.to_device_bf16(src, "cuda"), "separate")
+    dcache = K.PagedCache.from_tensors(dd, "separate")
+    t = lambda a: torch.from_numpy(a).cuda()
+    x = K.kv_build_xfer_list(t(off), t(ids), None, 2)
+    stage = K.kv_pack_blocks(scache, x, ids.shape[0], slice_off=s_off, slice_bytes=s_len)
+    K.kv_unpack_blocks(dcache, stage, x, ids.shape[0], 16, s_len, d_off, t(off), t(doff), t(dids))
+    torch.cuda.synchronize()
+    st = oracle.pack(H.ora_cache(sg, src), off, ids, s_off, s_len)
+    np.testing.assert_array_equal(stage.cpu().numpy(), st)
+    dh = [a.copy() for a in dst]
+    assert oracle.unpack(H.ora_cache(dg, dh), st, off, doff, dids, 16, s_len, d_off) == 0
+    for a, b in zip(dd, dh):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+    assert K.kv_get_last_error() == 0
+
+
+def test_reshape_padding_and_range():
+    g = W.CacheGeom("blocks_first", 12, 4, 2, 32)
+    rng = np.random.default_rng(9)
+    host = W.host_cache_tensors(g, 2, rng)
+    dev = W.to_device_bf16(host, "cuda")
+    cache = K.PagedCache.from_tensors(dev, "blocks_first")
+    T = 6
+    new = [torch.from_numpy(rng.integers(-2 ** 15, 2 ** 15, size=(T, 2, 32), dtype=np.int16)).cuda().view(
+        torch.bfloat16) for _ in range(4)]
+    slot = torch.tensor([5, -1, 47, 48, 0, 1000], dtype=torch.int64, device="cuda")  # 48 slots in the cache
+    K.kv_reshape_and_cache(cache, new, slot)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() & K.KV_DERR_SLOT
+    hc = [h.copy() for h in host]
+    rows = [n.cpu().view(torch.int16).numpy().view(np.uint8).reshape(T, -1) for n in new]
+    assert oracle.reshape_and_cache(H.ora_cache(g, hc), rows, np.array([5, -1, 47, -1, 0, -1])) == 0
+    for a, b in zip(dev, hc):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+
+
+def test_out_of_range_run_skipped():
+    """A run naming blocks past the cache is skipped and flagged; the other runs still land."""
+    g = W.CacheGeom("separate", 16, 4, 1, 64)
+    rng = np.random.default_rng(11)
+    host = W.host_cache_tensors(g, 1, rng)
+    cache = K.PagedCache.from_tensors(W.to_device_bf16(host, "cuda"), "separate")
+    off, ids = W.csr([[2, 3], [15, 16], [7]])  # 15,16 runs past the 16-block cache
+    x = K.kv_build_xfer_list(torch.from_numpy(off).cuda(), torch.from_numpy(ids).cuda())
+    stage = K.kv_pack_blocks(cache, x, ids.shape[0])
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() & K.KV_DERR_BLOCK
+    s = stage.cpu().numpy().reshape(5, -1)
+    h = host[0].reshape(16, -1).view(np.uint8)
+    np.testing.assert_array_equal(s[0], h[2])
+    np.testing.assert_array_equal(s[1], h[3])
+    np.testing.assert_array_equal(s[4], h[7])
+
+
+def test_host_argument_errors():
+    g = W.CacheGeom("separate", 8, 4, 1, 64)
+    dev = W.device_cache(g, 1, "cuda", seed=1)
+    cache = K.PagedCache.from_tensors(dev, "separate")
+    x = K.kv_build_xfer_list(torch.zeros(2, dtype=torch.int32, device="cuda").index_fill_(0, torch.tensor([1], device="cuda"), 1),
+                             torch.zeros(1, dtype=torch.int32, device="cuda"))
+    with pytest.raises(K.KvError) as e:
+        K.kv_pack_blocks(cache, x, 1, slice_off=8, slice_bytes=32)  # slice offset not 16-byte aligned
+    assert e.value.status == K.KV_ERR_ALIGN
+    with pytest.raises(K.KvError) as e:
+        K.kv_pack_blocks(cache, x, 1, slice_off=64, slice_bytes=128)  # slice past the row
+    assert e.value.status == K.KV_ERR_RANGE
+    with pytest.raises(K.KvError) as e:
+        K.kv_pack_blocks(cache, x, 1, stage=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == K.KV_ERR_RANGE
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() == 0

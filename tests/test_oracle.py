@@ -10,8 +10,8 @@ checks that every one of them fails at least one pin.
 from __future__ import annotations
 
 import os
-import re
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -389,19 +389,34 @@ MUTANTS = [
 ]
 
 
+_RUN_PINS = """
+import sys
+sys.path.insert(0, {root!r})
+import oracle
+from tests import test_oracle as T
+lib = oracle._get({so!r})
+failed = []
+for pin in T.PINS:
+    try:
+        pin(lib)
+    except (AssertionError, ValueError, IndexError):
+        failed.append(pin.__name__)
+print("FAILED:" + ",".join(failed))
+sys.exit(1 if failed else 0)
+"""
+
+
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_pins_catch_mutant(tmp_path, name, old, new):
+    """Each mutant runs the pins in a child process: a planted index mistake may also
+    corrupt memory, and a crash of the child counts as caught."""
     src = open(os.path.join(os.path.dirname(oracle.__file__), "pagedkv_oracle.c"), encoding="utf-8").read()
     assert old in src, f"mutation site missing: {old!r}"
     mut = tmp_path / "mutant.c"
     mut.write_text(src.replace(old, new), encoding="utf-8")
     so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", str(so), str(mut)], check=True)
-    lib = oracle._get(str(so))
-    failed = []
-    for pin in PINS:
-        try:
-            pin(lib)
-        except (AssertionError, ValueError, IndexError):
-            failed.append(pin.__name__)
-    assert failed, f"no pin caught mutant: {name}"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _RUN_PINS.format(root=root, so=str(so))], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode != 0, f"no pin caught mutant: {name}"
