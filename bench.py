@@ -1,0 +1,452 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one pass of the whole path over one batch of the page-shaped workload
+(48 layer tensors [147456, 2, 16, 1, 128] bf16, 8 prompts x 576 blocks):
+  kv_slot_mapping (73728 new tokens) -> kv_reshape_and_cache (48 layers) ->
+  kv_build_xfer_list (4608 blocks) -> kv_pack_blocks (1.81 GB staged) ->
+  kv_unpack_blocks (into the receiver's 147456-block cache at other block ids).
+value = algorithmic bytes of the step (payload read + written, index arrays) / step time,
+in GB/s, summed over ranks.  Inputs are larger than L2 (the step moves ~11 GB).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (weak scaling).
+--impl reference times the CPU oracle (the plain C statement of the same step) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_81_gb300 import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_NAMES = ("slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack")
+COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="page_shaped", choices=sorted(W.PRESETS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per pack launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "pack_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash(COPY_SOURCES) or workload not in d.get("per_launch_bytes", {}):
+        return None
+    return d["per_launch_bytes"][workload]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        self.t0 = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t_begin, t_end):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path:
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def config_dict(wl: W.Workload, case: W.Case, step=None) -> dict:
+    d = {"workload": wl.name, "layers": wl.n_layers, "tensors": wl.n_tensors, "layout": wl.src.layout,
+         "num_blocks": wl.src.num_blocks, "block_size": wl.src.block_size, "row_bytes": wl.src.row_bytes,
+         "requests": case.n_reqs, "blocks_listed": case.n_blocks, "new_tokens": case.n_tokens,
+         "payload_dtype": "bf16 (moved as opaque 16-byte vectors)",
+         "l2": "inputs larger than L2: no flush (each step moves several GB through a 129 MB L2)"}
+    if not wl.equal_geometry:
+        d.update(dst_block_size=wl.dst.block_size, slice_bytes=wl.moved_slice, slice_off=wl.slice_off)
+    if step is not None:
+        d["max_run_blocks"] = step.max_run_blocks
+    return d
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_cache_81_gb300 import build
+    build.build()
+    from paged_kv_cache_81_gb300 import pagedkv as K
+    from paged_kv_cache_81_gb300.step import TransferStep
+
+    wl = W.PRESETS[args.workload]
+    case = W.make_case(wl)
+    seed = wl.seed * 7919 + rank
+    src = W.device_cache(wl.src, wl.n_tensors, dev, seed=seed)
+    dst = W.device_cache(wl.dst, wl.n_tensors, dev, seed=seed + 1) if wl.kind != "mla" else None
+    new = W.new_token_rows(wl.src, wl.n_tensors, case.n_tokens, dev, seed=seed + 2)
+    step = TransferStep(wl, case, src, dst, new, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K.kv_get_last_error(clear=True)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def slot_mapping():
+        if step.n_tokens:
+            K.kv_slot_mapping(step.block_table, step.token_req, step.token_pos, step.src.block_size, step.slot)
+
+    def reshape_and_cache():
+        if step.n_tokens:
+            K.kv_reshape_and_cache(step.src, step.new_kv, step.slot)
+
+    # the five calls of step.run(), split so that each is bracketed by its own events
+    calls = [("slot_mapping", slot_mapping), ("reshape_and_cache", reshape_and_cache),
+             ("build_xfer_list", step.build), ("pack", step.pack), ("unpack", step.unpack)]
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize(dev)
+    err = K.kv_get_last_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(args.steps):
+        e = ev[s]
+        e[0].record(stream)
+        for k, (_, fn) in enumerate(calls):
+            fn()
+            e[k + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    elapsed_ms = start.elapsed_time(end)
+    per_kernel_ms = {name: statistics.mean(ev[s][k].elapsed_time(ev[s][k + 1]) for s in range(args.steps))
+                     for k, (name, _) in enumerate(calls)}
+    err = K.kv_get_last_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} in the timed region")
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    b = step.bytes()
+    per_bytes = {"slot_mapping": b.slot_mapping, "reshape_and_cache": b.reshape_and_cache,
+                 "build_xfer_list": b.build_xfer_list, "pack": b.pack, "unpack": b.unpack}
+    step_bytes = b.total
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    peak, peak_kind = peaks()
+    timed = {k: v for k, v in per_kernel_ms.items() if per_bytes[k] > 0}
+    dominant = max(timed, key=lambda k: timed[k])
+    achieved = per_bytes[dominant] / (per_kernel_ms[dominant] * 1e-3) / 1e9
+    traffic = ncu_traffic(wl.name) if dominant == "pack" else None
+    kernels = {}
+    for name in KERNEL_NAMES:
+        if per_bytes[name] == 0:
+            continue
+        ms = per_kernel_ms[name]
+        gbs = per_bytes[name] / (ms * 1e-3) / 1e9
+        kernels[name] = {"ms": round(ms, 4), "bytes": per_bytes[name], "gbs": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4)}
+    if step.n_tokens:
+        kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, case, step, dev, stream, K, world, barrier)
+
+    line = {
+        "metric": "KV pack/unpack GB/s moved and % of HBM peak; reshape_and_cache tokens/s",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8", "data": "synthetic (seeded random cache contents and block lists of the page-shaped workload)",
+        "config": config_dict(wl, case, step),
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+                     if peak_kind == "measured" else "of fallback", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": per_bytes[dominant]},
+        "kernels": kernels,
+        "gpu_launches": args.steps * step.launches_per_step,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, case, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
+    """The same step through the public API from pinned host buffers: copy the step's inputs
+    (new K/V rows, token and block lists) host->device, run the five calls, read the run
+    count and the device error word back to the host."""
+    import torch
+
+    host_inputs = []
+    if step.n_tokens:
+        buf = step.new_kv[0]._base  # all tensors' new rows share one device buffer
+        host_inputs.append((buf, torch.empty(buf.shape, dtype=buf.dtype, pin_memory=True)))
+        for t in (step.block_table, step.token_req, step.token_pos):
+            host_inputs.append((t, t.cpu().pin_memory()))
+    for t in (step.req_offsets, step.src_ids, step.dst_req_offsets, step.dst_ids):
+        host_inputs.append((t, t.cpu().pin_memory()))
+    if step.n_tokens:
+        host_inputs[0][1].copy_(host_inputs[0][0])  # same contents as the device step's rows
+    n_runs_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in host_inputs)
+    d2h = n_runs_host.numel() * 4 + 4
+
+    steps = max(1, min(args.steps, 100))
+
+    def one():
+        for d, h in host_inputs:
+            d.copy_(h, non_blocking=True)
+        step.run()
+        n_runs_host.copy_(step.xfer.n_runs, non_blocking=True)
+        if K.kv_get_last_error(clear=False) != 0:  # 4-byte read of the device error word; synchronises
+            raise RuntimeError("device error in the end-to-end step")
+
+    for _ in range(3):
+        one()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier()
+    secs = time.perf_counter() - t0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([secs], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+    value = world * step.bytes().total * steps / secs / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": round(secs / steps * 1e3, 4)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores: CPU baseline and the reference arm
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: `layers` layer tensors of the
+    full-size geometry (same block lists, same new tokens), on the host."""
+
+    def __init__(self, wl: W.Workload, case: W.Case, layers: int = 1):
+        import oracle
+
+        self.oracle = oracle
+        self.wl, self.case = wl, case
+        self.nt = min(wl.n_tensors, layers * wl.src.tensors_per_layer)
+        g = wl.src
+        st = g.byte_strides()
+        shape = (g.tensor_bytes,)
+        self.src = [np.ones(shape, dtype=np.uint8) for _ in range(self.nt)]  # touched, so no page faults are timed
+        self.src_cache = oracle.Cache(self.src, g.num_blocks, g.block_size, g.n_planes, st["block_stride"],
+                                      st["plane_stride"], st["token_stride"], g.row_bytes)
+        self.has_dst = wl.kind != "mla"
+        if self.has_dst:
+            d = wl.dst
+            ds = d.byte_strides()
+            self.dst = [np.ones((d.tensor_bytes,), dtype=np.uint8) for _ in range(self.nt)]
+            self.dst_cache = oracle.Cache(self.dst, d.num_blocks, d.block_size, d.n_planes, ds["block_stride"],
+                                          ds["plane_stride"], ds["token_stride"], d.row_bytes)
+        T = case.n_tokens
+        self.rows = [np.full((T, g.row_bytes), k, dtype=np.uint8) for k in range(self.nt * g.n_planes)] if T else []
+        # algorithmic bytes of one sampled step (same accounting as the GPU step, scaled to the sample)
+        payload = self.nt * case.n_blocks * g.n_planes * g.block_size * wl.moved_slice
+        self.bytes = (T * 20 if T else 0) + (self.nt * g.n_planes * T * g.row_bytes * 2 + T * 8 if T else 0) + \
+            case.n_blocks * 4 * (2 if (wl.equal_geometry and self.has_dst) else 1) + 2 * payload + \
+            (2 * payload if self.has_dst else 0)
+
+    def step(self):
+        o, wl, case = self.oracle, self.wl, self.case
+        if case.n_tokens:
+            slot, _ = o.slot_mapping(case.block_table, case.token_req, case.token_pos, wl.src.block_size)
+            o.reshape_and_cache(self.src_cache, self.rows, slot)
+        equal = wl.equal_geometry and self.has_dst
+        o.build_xfer_list(case.req_offsets, case.src_ids, case.dst_ids if equal else None, 0)
+        stage = o.pack(self.src_cache, case.req_offsets, case.src_ids, wl.slice_off, wl.moved_slice)
+        if self.has_dst:
+            o.unpack(self.dst_cache, stage, case.req_offsets, case.dst_req_offsets, case.dst_ids,
+                     wl.src.block_size, wl.moved_slice, wl.dst_slice_off)
+
+
+def cpu_baseline(wl, case, seconds: float) -> dict:
+    s = OracleSample(wl, case, layers=1)
+    s.step()  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        s.step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(s.bytes * n / el / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} steps of one layer ({s.nt} of {wl.n_tensors} tensors) of the {wl.name} step, "
+                      f"single-threaded C oracle, {el:.1f} s; host has {os.cpu_count()} cores"}
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return  # under torchrun only rank 0 runs the CPU oracle
+    wl = W.PRESETS[args.workload]
+    case = W.make_case(wl)
+    s = OracleSample(wl, case, layers=1)
+    for _ in range(max(1, args.warmup)):
+        s.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.step()
+    secs = time.perf_counter() - t0
+    value = s.bytes * args.steps / secs / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "KV pack/unpack GB/s moved and % of HBM peak; reshape_and_cache tokens/s",
+        "value": round(value, 3), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": config_dict(wl, case),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step is one layer ({s.nt} of {wl.n_tensors} tensors) of the {wl.name} "
+                                   f"step on the single-threaded C oracle; host has {os.cpu_count()} cores"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
