@@ -48,7 +48,23 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling captures)")
+    ap.add_argument("--num-blocks", type=int, default=None, help="override blocks per tensor (profiling captures)")
     return ap.parse_args()
+
+
+def workload(args) -> W.Workload:
+    """The named preset, optionally shrunk for a profiler capture (same lists, smaller cache)."""
+    from dataclasses import replace
+    wl = W.PRESETS[args.workload]
+    if args.layers:
+        wl = replace(wl, n_layers=args.layers)
+    if args.num_blocks:
+        wl = replace(wl, src=replace(wl.src, num_blocks=args.num_blocks),
+                     dst=replace(wl.dst, num_blocks=args.num_blocks))
+    if args.layers or args.num_blocks:
+        wl = replace(wl, name=f"{wl.name}[layers={wl.n_layers},num_blocks={wl.src.num_blocks}]")
+    return wl
 
 
 def peaks():
@@ -183,7 +199,7 @@ def run_ours(args):
     from paged_kv_cache_81_gb300 import pagedkv as K
     from paged_kv_cache_81_gb300.step import TransferStep
 
-    wl = W.PRESETS[args.workload]
+    wl = workload(args)
     case = W.make_case(wl)
     seed = wl.seed * 7919 + rank
     src = W.device_cache(wl.src, wl.n_tensors, dev, seed=seed)
@@ -280,7 +296,7 @@ def run_ours(args):
         "metric": "KV pack/unpack GB/s moved and % of HBM peak; reshape_and_cache tokens/s",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u8", "data": "synthetic (seeded random cache contents and block lists of the page-shaped workload)",
+        "dtype": "u8", "data": f"synthetic (seeded random cache contents and block lists of the {wl.name} workload)",
         "config": config_dict(wl, case, step),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
@@ -415,7 +431,7 @@ def cpu_baseline(wl, case, seconds: float) -> dict:
 def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return  # under torchrun only rank 0 runs the CPU oracle
-    wl = W.PRESETS[args.workload]
+    wl = workload(args)
     case = W.make_case(wl)
     s = OracleSample(wl, case, layers=1)
     for _ in range(max(1, args.warmup)):

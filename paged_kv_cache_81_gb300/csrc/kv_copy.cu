@@ -74,15 +74,22 @@ __global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_consta
         nr = p.run_capacity;
     }
     if (nr < 0) nr = 0;
-    const int64_t per_tensor = nr * p.max_pieces;
-    const int64_t items = per_tensor * p.n_tensors;
+    // Items are numbered piece-major: (piece, tensor, run).  Every run has a piece 0, so the
+    // first n_tensors * nr items are all non-empty and spread evenly over the warps.
+    const int64_t per_piece = nr * p.n_tensors;
+    const int64_t items = per_piece * p.max_pieces;
 
-    for (int64_t item = warp; item < items; item += n_warps) {
-        const int32_t t = (int32_t)(item / per_tensor);
-        const int64_t rest = item - (int64_t)t * per_tensor;
-        const int64_t k = rest / p.max_pieces;
-        const int32_t piece = (int32_t)(rest - k * p.max_pieces);
-        const kv_xfer_run run = p.runs[k];
+    int64_t item = warp;
+    kv_xfer_run next;
+    if (item < items) next = p.runs[item % per_piece % nr];
+    while (item < items) {
+        const int64_t cur = item;
+        const kv_xfer_run run = next;
+        item += n_warps;
+        if (item < items) next = p.runs[item % per_piece % nr];  // prefetch: overlaps the copy below
+        const int32_t piece = (int32_t)(cur / per_piece);
+        const int64_t rest = cur - (int64_t)piece * per_piece;
+        const int32_t t = (int32_t)(rest / nr);
 
         const uint64_t item_chunks64 = (uint64_t)(int64_t)run.n_blocks * p.chunks_per_block;
         const uint64_t c_begin = (uint64_t)piece * kPieceChunks;

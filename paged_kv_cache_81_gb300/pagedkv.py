@@ -296,6 +296,8 @@ def kv_get_last_error(clear: bool = True, stream=None) -> int:
     return out.value
 
 
-def default_max_run_blocks(stage_block_bytes: int, target_bytes: int = 64 * 1024) -> int:
-    """A run cap that keeps one run at or under target_bytes per tensor (at least one block)."""
+def default_max_run_blocks(stage_block_bytes: int, target_bytes: int = 16 * 1024) -> int:
+    """A run cap that keeps one run at or under target_bytes per tensor (at least one block).
+
+    16 KiB is the piece a copy kernel hands to one warp, so a capped run is never split."""
     return max(1, int(target_bytes) // max(1, int(stage_block_bytes)))
