@@ -195,6 +195,33 @@ KV_API int kv_build_xfer_list(const int32_t *req_offsets, int32_t n_reqs, const 
                        void *workspace, int64_t workspace_bytes, kv_stream_t stream);
 
 /*
+ * kv_build_xfer_list_static - the pages have no counterpart to this entry point.
+ * It is kv_build_xfer_list with the same arguments and results, except that it needs no
+ * workspace: its look-back scratch is a fixed array of KV_XFER_STATIC_SCRATCH_BYTES
+ * (64 KiB) inside libpagedkv.so, held by every GPU that loads the library until the
+ * process exits.  It is for callers that cannot allocate device memory at the moment
+ * they build a transfer list: a transport's progress thread, where cudaMalloc and
+ * cudaFree may synchronise the device and stall the model's stream, or a serving
+ * process whose KV-cache pool already reserved nearly all free device memory, where
+ * even a small allocation can fail.  Nothing here calls cudaMalloc, cudaFree or any
+ * allocating routine; the caller still passes the inputs and the runs / n_runs outputs.
+ *  - n_blocks above KV_XFER_STATIC_MAX_BLOCKS is rejected with KV_ERR_RANGE before
+ *    anything is queued.
+ *  - The first call on each device looks up the array's device address with
+ *    cudaGetSymbolAddress (with that device current) and caches it; make that first call
+ *    before any stream capture.
+ *  - Every call clears the part of the array it uses on `stream` before its kernel runs.
+ *    All calls on a device share the one array, so calls that overlap on the GPU (on
+ *    different streams without ordering) race and produce garbage; order them.
+ */
+#define KV_XFER_STATIC_SCRATCH_BYTES 65536
+#define KV_XFER_STATIC_MAX_BLOCKS 4177920 /* 2040 tiles of 2048 entries: (65536 - 256) / 32 */
+KV_API int kv_build_xfer_list_static(const int32_t *req_offsets, int32_t n_reqs, const int32_t *src_ids,
+                                     const int32_t *dst_ids, int64_t n_blocks, int32_t max_run_blocks,
+                                     kv_xfer_run *runs, int64_t run_capacity, int32_t *n_runs,
+                                     kv_stream_t stream);
+
+/*
  * kv_pack_blocks [N section 2.4 extract_kv_from_layer, F section 1.2]: for every
  * tensor t and run of `runs`, copies rows (t, src_block + m, p, o) - byte slice
  * [src_slice_off, src_slice_off + stage->slice_bytes) of each row - to the staging

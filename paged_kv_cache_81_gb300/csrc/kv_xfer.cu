@@ -17,6 +17,7 @@
 // The cap's starts in a stretch [a, b) with no natural start, continuing a run opened at
 // s < a, are counted in closed form: floor((b-1-s)/cap) - floor((a-1-s)/cap).
 #include <algorithm>
+#include <mutex>
 
 #include "kv_common.cuh"
 
@@ -377,3 +378,87 @@ int kv_build_xfer_list(const int32_t *req_offsets, int32_t n_reqs, const int32_t
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kv_build_xfer_list_static: the builder above with its look-back scratch in a fixed
+// array inside this library instead of a workspace the caller allocates.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kStaticScratchBytes = KV_XFER_STATIC_SCRATCH_BYTES;
+static_assert(kHeaderBytes + ((KV_XFER_STATIC_MAX_BLOCKS + kTile - 1) / kTile) * (int64_t)sizeof(TileRecord) <=
+                  kStaticScratchBytes,
+              "KV_XFER_STATIC_MAX_BLOCKS does not fit the static scratch");
+static_assert(kHeaderBytes + ((KV_XFER_STATIC_MAX_BLOCKS + kTile) / kTile) * (int64_t)sizeof(TileRecord) >
+                  kStaticScratchBytes,
+              "KV_XFER_STATIC_MAX_BLOCKS is not the largest list the static scratch holds");
+
+// One copy per device that loads this library, kept until the process exits.  Every
+// kv_build_xfer_list_static call on that device uses it.
+static __device__ __align__(256) uint8_t g_xfer_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mutex;
+void *g_static_scratch_addr[kMaxStaticDevices];
+
+// Device address of the scratch array on the current device.  In host code the array's
+// name stands for a host-side shadow, so the address is looked up once per device (with
+// that device current) and cached.
+int static_scratch_address(int device, void **out)
+{
+    if (device < 0 || device >= kMaxStaticDevices) return KV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_scratch_addr[device] == nullptr) {
+        void *p = nullptr;
+        const int st = pkv::cuda_status(cudaGetSymbolAddress(&p, g_xfer_static_scratch));
+        if (st != KV_OK) return st;
+        g_static_scratch_addr[device] = p;
+    }
+    *out = g_static_scratch_addr[device];
+    return KV_OK;
+}
+
+}  // namespace
+
+extern "C" int kv_build_xfer_list_static(const int32_t *req_offsets, int32_t n_reqs, const int32_t *src_ids,
+                                         const int32_t *dst_ids, int64_t n_blocks, int32_t max_run_blocks,
+                                         kv_xfer_run *runs, int64_t run_capacity, int32_t *n_runs,
+                                         kv_stream_t stream)
+{
+    if (n_reqs < 0 || n_blocks < 0 || max_run_blocks < 0 || run_capacity < 0 || n_runs == nullptr ||
+        req_offsets == nullptr)
+        return KV_ERR_INVALID_ARG;
+    if (n_blocks > KV_XFER_STATIC_MAX_BLOCKS) return KV_ERR_RANGE;
+    if (n_blocks > 0 && (n_reqs == 0 || src_ids == nullptr || (run_capacity > 0 && runs == nullptr)))
+        return KV_ERR_INVALID_ARG;
+    if (((uintptr_t)runs & 7u) != 0) return KV_ERR_ALIGN;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (n_blocks == 0) return pkv::cuda_status(cudaMemsetAsync(n_runs, 0, sizeof(int32_t), s));
+    const pkv::DeviceInfo *dev = pkv::current_device();
+    if (dev == nullptr) return KV_ERR_CUDA;
+    void *scratch = nullptr;
+    int st = static_scratch_address(dev->device, &scratch);
+    if (st != KV_OK) return st;
+
+    int64_t need = 0;
+    kv_xfer_workspace_bytes(n_blocks, &need);
+    // the tile counter and the tile records must start at zero; the array keeps the last call's contents
+    st = pkv::cuda_status(cudaMemsetAsync(scratch, 0, (size_t)need, s));
+    if (st != KV_OK) return st;
+    XferParams p{};
+    p.req_offsets = req_offsets;
+    p.src = src_ids;
+    p.dst = dst_ids;
+    p.runs = runs;
+    p.n_runs = n_runs;
+    p.counter = reinterpret_cast<uint32_t *>(scratch);
+    p.tiles = reinterpret_cast<TileRecord *>(reinterpret_cast<uint8_t *>(scratch) + kHeaderBytes);
+    p.err = dev->err_word;
+    p.capacity = run_capacity;
+    p.n_reqs = n_reqs;
+    p.n = (int32_t)n_blocks;
+    p.cap = max_run_blocks;
+    const int tiles = (int)((n_blocks + kTile - 1) / kTile);
+    build_xfer_kernel<<<tiles, kThreads, 0, s>>>(p);
+    return pkv::cuda_status(cudaGetLastError());
+}

@@ -25,7 +25,7 @@ KV_DERR_CAPACITY, KV_DERR_STAGE, KV_DERR_DST_TABLE, KV_DERR_TIMEOUT = 0x10, 0x20
 RUN_WORDS = 6  # a kv_xfer_run is 24 bytes: six int32 words (the last two hold the int64 stage_block)
 EXPORTS = ("kv_version", "kv_status_string", "kv_last_cuda_error", "kv_slot_mapping", "kv_reshape_and_cache",
            "kv_xfer_workspace_bytes", "kv_build_xfer_list", "kv_pack_blocks", "kv_unpack_blocks",
-           "kv_get_last_error")
+           "kv_get_last_error", "kv_build_xfer_list_static")
 
 
 class KvError(RuntimeError):
@@ -85,6 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "kv_pack_blocks": ([D, i32, S, P, P, i64, i32, P, i64, P], ctypes.c_int),
             "kv_unpack_blocks": ([D, i32, S, P, P, i64, i32, P, i64, P, P, P, i32, P], ctypes.c_int),
             "kv_get_last_error": ([ctypes.POINTER(i32), i32, P], ctypes.c_int),
+            "kv_build_xfer_list_static": ([P, i32, P, P, i64, i32, P, i64, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -258,6 +259,27 @@ def kv_build_xfer_list(req_offsets: torch.Tensor, src_ids: torch.Tensor, dst_ids
     _check("kv_build_xfer_list", load().kv_build_xfer_list(
         _ptr(req_offsets), req_offsets.shape[0] - 1, _ptr(src_ids), _ptr(dst_ids), n, int(max_run_blocks),
         _ptr(out.runs), out.capacity, _ptr(out.n_runs), _ptr(workspace), workspace.numel(), _stream(stream)))
+    out.max_run_blocks = int(max_run_blocks)
+    return out
+
+
+KV_XFER_STATIC_MAX_BLOCKS = 4177920
+
+
+def kv_build_xfer_list_static(req_offsets: torch.Tensor, src_ids: torch.Tensor,
+                              dst_ids: Optional[torch.Tensor] = None, max_run_blocks: int = 0,
+                              out: Optional[XferList] = None, stream=None) -> XferList:
+    """kv_build_xfer_list without a workspace: the library's own fixed scratch array is used,
+    so the call itself allocates nothing (the outputs are still the caller's)."""
+    _i32(req_offsets, "req_offsets"), _i32(src_ids, "src_ids")
+    if dst_ids is not None:
+        _i32(dst_ids, "dst_ids")
+    n = src_ids.shape[0]
+    if out is None:
+        out = XferList(n, src_ids.device, max_run_blocks)
+    _check("kv_build_xfer_list_static", load().kv_build_xfer_list_static(
+        _ptr(req_offsets), req_offsets.shape[0] - 1, _ptr(src_ids), _ptr(dst_ids), n, int(max_run_blocks),
+        _ptr(out.runs), out.capacity, _ptr(out.n_runs), _stream(stream)))
     out.max_run_blocks = int(max_run_blocks)
     return out
 
