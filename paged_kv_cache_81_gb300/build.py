@@ -42,17 +42,18 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = LIB, objdir: str = BUILD) -> str:
+    """Compile and link; `out`/`objdir` and `extra_flags` (e.g. -D tuning macros) build variants."""
     srcs = sources()
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
-    if not force and not _stale(LIB, srcs + headers + [__file__]):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and not _stale(out, srcs + headers + [__file__]):
+        return out
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for s in srcs:
-        obj = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(s)[:-3] + ".o")
         objs.append(obj)
         cmd = [cc, "-c", s, "-o", obj] + ARCH + NVCC_FLAGS + list(extra_flags)
         if verbose:
@@ -60,20 +61,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         procs.append((s, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     failed = []
     for s, p in procs:
-        out, _ = p.communicate()
+        log, _ = p.communicate()
         if p.returncode != 0:
-            failed.append((s, out.decode(errors="replace")))
-        elif (verbose or extra_flags) and out:
-            print(out.decode(errors="replace"), file=sys.stderr)
+            failed.append((s, log.decode(errors="replace")))
+        elif (verbose or extra_flags) and log:
+            print(log.decode(errors="replace"), file=sys.stderr)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"{s}:\n{o}" for s, o in failed))
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     link = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

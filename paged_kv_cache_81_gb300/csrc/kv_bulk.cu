@@ -1,0 +1,285 @@
+// TMA bulk-copy engine for kv_pack_blocks / kv_unpack_blocks when every block of the cache
+// is one contiguous span (the MERGED and BLOCKS address modes).
+//
+// Each run of the xfer_list (page "5. flagcx connector design & dev & test", section 1.2:
+// one transfer per contiguous group) becomes one or more bulk copies of at most kStage
+// bytes: global -> shared memory with cp.async.bulk (completion counted on an mbarrier),
+// then shared memory -> global with cp.async.bulk (bulk-group completion).  The copy
+// itself is done by the SM's TMA unit; no register ever holds payload.
+//
+// One issuing lane per warp ("pipe") owns a ring of kSlots shared-memory slots.  A pipe
+// keeps up to kSlots - 1 loads in flight: before it loads into a slot it stores the oldest
+// loaded slot, then waits until all but the newest store have finished reading shared
+// memory, which frees the slot the new load takes.  The other lanes of the warp fetch the
+// next 32 run records while the issuing lane works through the current 32.
+// Every mbarrier wait is bounded (2 s of globaltimer); a timeout sets KV_DERR_TIMEOUT,
+// stops issuing, waits (bounded again) for the loads in flight and returns.
+#include <algorithm>
+#include <mutex>
+
+#include "kv_copy.cuh"
+
+#ifndef PKV_BULK_STAGE_BYTES
+#define PKV_BULK_STAGE_BYTES 8192
+#endif
+#ifndef PKV_BULK_SLOTS
+#define PKV_BULK_SLOTS 3
+#endif
+#ifndef PKV_BULK_PIPES
+#define PKV_BULK_PIPES 8
+#endif
+
+namespace {
+
+using pkv::CopyParams;
+
+constexpr uint32_t kStage = PKV_BULK_STAGE_BYTES;  // bytes per slot (multiple of 16)
+constexpr int kSlots = PKV_BULK_SLOTS;
+constexpr int kPipes = PKV_BULK_PIPES;  // warps (pipes) per CTA
+constexpr int kBatch = 32;             // run records fetched per warp round
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+static_assert(kStage % 16 == 0 && kSlots >= 3, "bulk engine shape");
+
+struct PipeState {  // per pipe, in shared memory after the slot data
+    uint64_t bar[kSlots];
+    uint64_t dst[kSlots];
+    uint32_t bytes[kSlots];
+    kv_xfer_run rec[kBatch];
+};
+
+constexpr size_t kSmemBytes = (size_t)kPipes * kSlots * kStage + (size_t)kPipes * sizeof(PipeState);
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long now_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false after kWaitLimitNs.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = now_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (now_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_smem),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// The issuing lane's view of one pipe.
+struct Pipe {
+    uint32_t data;  // shared address of slot 0
+    PipeState *st;
+    uint32_t head = 0;  // next op to store
+    uint32_t tail = 0;  // next op to load
+    bool failed = false;
+    int *err;
+
+    __device__ uint32_t bar(int s) const { return smem_addr(&st->bar[s]); }
+
+    __device__ void store_oldest()
+    {
+        const int s = (int)(head % kSlots);
+        if (!mbar_wait(bar(s), (head / kSlots) & 1u)) {
+            failed = true;
+            pkv::set_error(err, KV_DERR_TIMEOUT);
+            return;
+        }
+        bulk_store(reinterpret_cast<void *>(st->dst[s]), data + (uint32_t)s * kStage, st->bytes[s]);
+        bulk_commit();
+        head++;
+    }
+
+    __device__ void push(const uint8_t *src, uint8_t *dst, uint32_t bytes)
+    {
+        if (failed) return;
+        if (tail - head == kSlots - 1) {
+            store_oldest();
+            if (failed) return;
+            bulk_wait_read_1();  // every store but the newest has read its slot
+        }
+        const int s = (int)(tail % kSlots);
+        st->dst[s] = reinterpret_cast<uint64_t>(dst);
+        st->bytes[s] = bytes;
+        mbar_arrive_expect_tx(bar(s), bytes);
+        bulk_load(data + (uint32_t)s * kStage, src, bytes, bar(s));
+        tail++;
+    }
+
+    __device__ void span(const uint8_t *src, uint8_t *dst, int64_t bytes)
+    {
+        for (int64_t off = 0; off < bytes; off += kStage)
+            push(src + off, dst + off, (uint32_t)std::min<int64_t>(kStage, bytes - off));
+    }
+
+    __device__ void drain()
+    {
+        while (!failed && head != tail) store_oldest();
+        if (failed) {  // let the loads still in flight land before shared memory goes away
+            for (uint32_t i = head; i != tail; i++) mbar_wait(bar((int)(i % kSlots)), (i / kSlots) & 1u);
+        }
+        bulk_wait_all();
+    }
+};
+
+template <bool MERGE, bool PACK>
+__global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_constant__ CopyParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    PipeState *st = reinterpret_cast<PipeState *>(smem + (size_t)kPipes * kSlots * kStage) + w;
+
+    Pipe pipe;
+    pipe.data = smem_addr(smem + (size_t)w * kSlots * kStage);
+    pipe.st = st;
+    pipe.err = p.err;
+    if (lane == 0) {
+        for (int s = 0; s < kSlots; s++) mbar_init(pipe.bar(s), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+
+    int64_t nr = *p.n_runs;
+    if (nr > p.run_capacity) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) pkv::set_error(p.err, KV_DERR_CAPACITY);
+        nr = p.run_capacity;
+    }
+    if (nr < 0) nr = 0;
+    const int64_t items = nr * p.n_tensors;  // item = tensor * nr + run, tensor-major
+    const int64_t g = (int64_t)blockIdx.x * kPipes + w;
+    const int64_t P = (int64_t)gridDim.x * kPipes;
+    const int64_t block_bytes = p.stage_block_bytes;
+
+    kv_xfer_run next{};
+    {
+        const int64_t it = g + (int64_t)lane * P;
+        if (it < items) next = p.runs[it % nr];
+    }
+    for (int64_t round = 0; g + round * kBatch * P < items; round++) {
+        st->rec[lane] = next;
+        __syncwarp();
+        {
+            const int64_t it = g + ((round + 1) * kBatch + lane) * P;  // prefetch the next round
+            if (it < items) next = p.runs[it % nr];
+        }
+        if (lane == 0 && !pipe.failed) {
+            for (int i = 0; i < kBatch; i++) {
+                const int64_t item = g + (round * kBatch + i) * P;
+                if (item >= items) break;
+                const int32_t t = (int32_t)(item / nr);
+                const kv_xfer_run run = st->rec[i];
+                if (run.n_blocks <= 0) continue;
+                if (run.stage_block < 0 || run.stage_block + run.n_blocks > p.n_stage_blocks) {
+                    pkv::set_error(p.err, KV_DERR_STAGE);
+                    continue;
+                }
+                const int64_t blk = PACK ? run.src_block : run.dst_block;
+                if (blk < 0 || blk + run.n_blocks > p.num_blocks) {
+                    pkv::set_error(p.err, KV_DERR_BLOCK);
+                    continue;
+                }
+                uint8_t *const cache = reinterpret_cast<uint8_t *>(p.base[t]) + blk * p.block_stride;
+                uint8_t *const stage =
+                    p.stage + (int64_t)(p.tensor_begin + t) * p.stage_tensor_bytes + run.stage_block * block_bytes;
+                if (MERGE) {
+                    const int64_t bytes = (int64_t)run.n_blocks * block_bytes;
+                    if (PACK) pipe.span(cache, stage, bytes);
+                    else pipe.span(stage, cache, bytes);
+                } else {
+                    for (int32_t m = 0; m < run.n_blocks; m++) {
+                        uint8_t *c = cache + (int64_t)m * p.block_stride;
+                        uint8_t *sg = stage + (int64_t)m * block_bytes;
+                        if (PACK) pipe.span(c, sg, block_bytes);
+                        else pipe.span(sg, c, block_bytes);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    }
+    if (lane == 0) pipe.drain();
+    __syncwarp();
+}
+
+using BulkFn = void (*)(CopyParams);
+
+BulkFn pick(int mode, bool pack)
+{
+    if (mode == pkv::MERGED) return pack ? bulk_copy_kernel<true, true> : bulk_copy_kernel<true, false>;
+    return pack ? bulk_copy_kernel<false, true> : bulk_copy_kernel<false, false>;
+}
+
+}  // namespace
+
+namespace pkv {
+
+int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s)
+{
+    static std::mutex mu;
+    static bool configured[64][2][2];
+    static int per_sm[64][2][2];
+    const BulkFn fn = pick(mode, pack);
+    const int m = mode == MERGED ? 1 : 0, d = pack ? 1 : 0, di = dev.device & 63;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[di][m][d]) {
+            int st = cuda_status(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
+            if (st != KV_OK) return st;
+            int n = 0;
+            st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kPipes * 32, kSmemBytes));
+            if (st != KV_OK) return st;
+            per_sm[di][m][d] = std::max(1, n);
+            configured[di][m][d] = true;
+        }
+    }
+    fn<<<dev.num_sms * per_sm[di][m][d], kPipes * 32, kSmemBytes, s>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace pkv

@@ -18,49 +18,24 @@
 //   ROWS    row by row: a head slice, a strided token dimension, or kv-first planes
 //   REMAP   unpack onto another block size / another block list (token granular)
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
-#include "kv_common.cuh"
+#include "kv_copy.cuh"
 
 namespace {
 
+using pkv::CopyParams;
 using pkv::FastDiv;
+using pkv::MERGED;
+using pkv::BLOCKS;
+using pkv::ROWS;
+using pkv::REMAP;
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
 constexpr uint32_t kPieceChunks = 1024;  // 16 KiB
-
-enum Mode { MERGED = 0, BLOCKS = 1, ROWS = 2, REMAP = 3 };
-
-struct CopyParams {
-    const kv_xfer_run *runs;
-    const int32_t *n_runs;
-    int64_t run_capacity;
-    uint8_t *stage;
-    int64_t stage_tensor_bytes;  // n_stage_blocks * stage_block_bytes
-    int64_t stage_block_bytes;   // planes * bs * slice
-    int64_t n_stage_blocks;
-    int64_t num_blocks;  // cache blocks per tensor
-    int64_t block_stride;
-    int64_t plane_stride;
-    int64_t token_stride;
-    int32_t row_off;  // byte offset of the slice inside a cache row
-    int32_t n_tensors;
-    int32_t tensor_begin;
-    int32_t max_pieces;
-    uint32_t chunks_per_block;  // staged block / 16
-    FastDiv div_cpr;            // chunks per staged row
-    FastDiv div_bs;             // staged (source) block size
-    FastDiv div_rpb;            // staged rows per block = planes * bs
-    FastDiv div_cpb;            // chunks per staged block
-    FastDiv div_dbs;            // destination block size (REMAP)
-    const int32_t *src_req_offsets;
-    const int32_t *dst_req_offsets;
-    const int32_t *dst_ids;
-    int32_t n_reqs;
-    int *err;
-    uint64_t base[pkv::kMaxTensorsPerLaunch];
-};
 
 template <int MODE, bool PACK>
 __global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_constant__ CopyParams p)
@@ -219,6 +194,23 @@ int resident_ctas(int device, int mode, bool pack)
     return slot;
 }
 
+// Copy engine for whole contiguous blocks.  The TMA bulk-copy engine (kv_bulk.cu) moves
+// blocks of 16 KiB and more faster than the register-staged warp engine above; for smaller
+// blocks the two measure within noise of each other and the warp engine is kept.
+// PAGEDKV_COPY_ENGINE=lsu|bulk (read once) forces one engine for measurements.
+bool bulk_engine(int64_t block_bytes)
+{
+    static const int forced = [] {
+        const char *e = std::getenv("PAGEDKV_COPY_ENGINE");
+        if (e == nullptr) return 0;
+        if (std::strcmp(e, "bulk") == 0) return 1;
+        if (std::strcmp(e, "lsu") == 0) return 2;
+        return 0;
+    }();
+    if (forced) return forced == 1;
+    return block_bytes >= 16 * 1024;
+}
+
 bool block_contiguous(const kv_cache_desc *c, int32_t row_off, int32_t slice)
 {
     return row_off == 0 && slice == c->row_bytes && c->token_stride == c->row_bytes &&
@@ -263,15 +255,21 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     const int64_t run_chunks = (int64_t)std::max(1, max_run_blocks) * cpb;
     p.max_pieces = max_run_blocks > 0 ? (int32_t)std::min<int64_t>((run_chunks + kPieceChunks - 1) / kPieceChunks, 1 << 20) : 1;
 
+    const bool bulk = (mode == MERGED || mode == BLOCKS) && bulk_engine(stage_block_bytes);
     const KernelFn fn = pick(mode, pack);
-    const int grid = dev->num_sms * resident_ctas(dev->device, mode, pack);
+    const int grid = bulk ? 0 : dev->num_sms * resident_ctas(dev->device, mode, pack);
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
         const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
         p.n_tensors = nt;
         p.tensor_begin = t0;
         for (int32_t t = 0; t < nt; t++) p.base[t] = cache->base[t0 + t];
-        fn<<<grid, kThreads, 0, s>>>(p);
-        const int st = pkv::cuda_status(cudaGetLastError());
+        int st;
+        if (bulk) {
+            st = pkv::launch_bulk_copy(p, mode, pack, *dev, s);
+        } else {
+            fn<<<grid, kThreads, 0, s>>>(p);
+            st = pkv::cuda_status(cudaGetLastError());
+        }
         if (st != KV_OK) return st;
     }
     return KV_OK;

@@ -1,0 +1,43 @@
+// Shared between the copy engines of kv_pack_blocks / kv_unpack_blocks (not part of the ABI).
+#pragma once
+
+#include "kv_common.cuh"
+
+namespace pkv {
+
+enum CopyMode { MERGED = 0, BLOCKS = 1, ROWS = 2, REMAP = 3 };
+
+struct CopyParams {
+    const kv_xfer_run *runs;
+    const int32_t *n_runs;
+    int64_t run_capacity;
+    uint8_t *stage;
+    int64_t stage_tensor_bytes;  // n_stage_blocks * stage_block_bytes
+    int64_t stage_block_bytes;   // planes * bs * slice
+    int64_t n_stage_blocks;
+    int64_t num_blocks;  // cache blocks per tensor
+    int64_t block_stride;
+    int64_t plane_stride;
+    int64_t token_stride;
+    int32_t row_off;  // byte offset of the slice inside a cache row
+    int32_t n_tensors;
+    int32_t tensor_begin;
+    int32_t max_pieces;
+    uint32_t chunks_per_block;  // staged block / 16
+    FastDiv div_cpr;            // chunks per staged row
+    FastDiv div_bs;             // staged (source) block size
+    FastDiv div_rpb;            // staged rows per block = planes * bs
+    FastDiv div_cpb;            // chunks per staged block
+    FastDiv div_dbs;            // destination block size (REMAP)
+    const int32_t *src_req_offsets;
+    const int32_t *dst_req_offsets;
+    const int32_t *dst_ids;
+    int32_t n_reqs;
+    int *err;
+    uint64_t base[kMaxTensorsPerLaunch];
+};
+
+// Launches the TMA bulk-copy engine for a MERGED or BLOCKS copy (kv_bulk.cu).
+int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s);
+
+}  // namespace pkv

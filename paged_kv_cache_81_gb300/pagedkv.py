@@ -16,7 +16,7 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+LIB_PATH = os.environ.get("PAGEDKV_LIB") or os.path.join(_HERE, "libpagedkv.so")
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_ALIGN, KV_ERR_RANGE, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_ERR_UNSUPPORTED = range(7)
 KV_DERR_TABLE, KV_DERR_SLOT, KV_DERR_BLOCK, KV_DERR_LIST = 0x01, 0x02, 0x04, 0x08
