@@ -35,7 +35,8 @@ from paged_kv_cache_81_gb300 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_NAMES = ("slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack")
-COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
+COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_copy.cuh",
+                "paged_kv_cache_81_gb300/csrc/kv_bulk.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
 
 
 def parse():
@@ -86,16 +87,18 @@ def source_hash(paths) -> str:
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per pack launch from the committed ncu summary, if the kernel source is unchanged."""
-    path = os.path.join(ROOT, "profiles", "pack_traffic.json")
+    """DRAM bytes (read + write) per pack launch from the committed ncu summary of this workload,
+    or None when the summary is missing or the copy kernels' source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{workload}_pack_dram.md")
     try:
         with open(path) as f:
-            d = json.load(f)
-    except Exception:
+            text = f.read()
+    except OSError:
         return None
-    if d.get("source_hash") != source_hash(COPY_SOURCES) or workload not in d.get("per_launch_bytes", {}):
+    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("source_hash:", "pack_dram_bytes_per_launch:")))
+    if fields.get("source_hash", "").strip() != source_hash(COPY_SOURCES):
         return None
-    return d["per_launch_bytes"][workload]
+    return int(fields["pack_dram_bytes_per_launch"].strip())
 
 
 class ClockSampler:
