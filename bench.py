@@ -169,6 +169,18 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
+def reduce_max(x: float, device) -> float:
+    """The maximum of x over all ranks (x itself without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def config_dict(wl: W.Workload, case: W.Case, step=None) -> dict:
     d = {"workload": wl.name, "layers": wl.n_layers, "tensors": wl.n_tensors, "layout": wl.src.layout,
          "num_blocks": wl.src.num_blocks, "block_size": wl.src.block_size, "row_bytes": wl.src.row_bytes,
@@ -263,10 +275,7 @@ def run_ours(args):
     if err:
         raise RuntimeError(f"device error word {err:#x} in the timed region")
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(elapsed_ms, dev)
 
     b = step.bytes()
     per_bytes = {"slot_mapping": b.slot_mapping, "reshape_and_cache": b.reshape_and_cache,
@@ -360,11 +369,7 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
     torch.cuda.synchronize(dev)
     barrier()
     secs = time.perf_counter() - t0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([secs], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = reduce_max(secs, dev)
     value = world * step.bytes().total * steps / secs / 1e9
     return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(secs / steps * 1e3, 4)}
