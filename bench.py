@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--stage", default="device", choices=["device", "host"],
+                    help="staging buffer in HBM, or in pinned host memory (pack/unpack over the host link)")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling captures)")
     ap.add_argument("--num-blocks", type=int, default=None, help="override blocks per tensor (profiling captures)")
     return ap.parse_args()
@@ -220,7 +222,7 @@ def run_ours(args):
     src = W.device_cache(wl.src, wl.n_tensors, dev, seed=seed)
     dst = W.device_cache(wl.dst, wl.n_tensors, dev, seed=seed + 1) if wl.kind != "mla" else None
     new = W.new_token_rows(wl.src, wl.n_tensors, case.n_tokens, dev, seed=seed + 2)
-    step = TransferStep(wl, case, src, dst, new, device=dev)
+    step = TransferStep(wl, case, src, dst, new, device=dev, host_stage=args.stage == "host")
     stream = torch.cuda.current_stream(dev)
     K.kv_get_last_error(clear=True)
 
@@ -301,6 +303,17 @@ def run_ours(args):
     if step.n_tokens:
         kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
 
+    host_link = None
+    if args.stage == "host":
+        # the bound of pack/unpack with host staging: device<->pinned copies of the staging size
+        host_link = measure_host_link(step.stage, dev, stream)
+        payload = per_bytes["pack"] // 2
+        host_link["pack_gbs"] = round(payload / (per_kernel_ms["pack"] * 1e-3) / 1e9, 1)
+        host_link["pack_frac_of_d2h"] = round(host_link["pack_gbs"] / host_link["d2h_gbs"], 4)
+        if per_bytes["unpack"]:
+            host_link["unpack_gbs"] = round(payload / (per_kernel_ms["unpack"] * 1e-3) / 1e9, 1)
+            host_link["unpack_frac_of_h2d"] = round(host_link["unpack_gbs"] / host_link["h2d_gbs"], 4)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, case, step, dev, stream, K, world, barrier)
@@ -321,12 +334,34 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
     }
+    if host_link is not None:
+        line["host_link"] = host_link
+        line["config"]["stage"] = "pinned host memory"
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, case, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_host_link(host_buf, dev, stream, reps: int = 5) -> dict:
+    """Device->host and host->device copy bandwidth (one direction's bytes) of a pinned buffer."""
+    import torch
+
+    d = torch.empty(host_buf.numel(), dtype=torch.uint8, device=dev)
+    out = {}
+    for name, (dst, src) in (("d2h_gbs", (host_buf, d)), ("h2d_gbs", (d, host_buf))):
+        dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = round(host_buf.numel() * reps / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    del d
+    return out
 
 
 def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):

@@ -230,7 +230,11 @@ KV_API int kv_build_xfer_list_static(const int32_t *req_offsets, int32_t n_reqs,
  * device memory as written by kv_build_xfer_list; at most run_capacity runs are read
  * (KV_DERR_CAPACITY if *n_runs is larger).  max_run_blocks is the cap the runs were
  * built with (0 if uncapped): runs are split into pieces of at most 16 KiB for the
- * warps by it; a longer run is still copied whole.  stage: device, stage_bytes bytes, at least
+ * warps by it; a longer run is still copied whole.  stage_buf: device memory, or pinned
+ * host memory (cudaHostAlloc / cudaHostRegister) when the payload is to be spilled to the
+ * host as the NCCL page's receiver does past its buffer threshold [N section 2.3]; the
+ * copy then runs over the host link.  Unregistered host memory is KV_ERR_INVALID_ARG.
+ * stage_bytes bytes, at least
  * n_tensors * n_blocks * n_planes * block_size * slice_bytes.  A run outside the cache
  * (KV_DERR_BLOCK) or the staging range (KV_DERR_STAGE) is skipped.
  */
@@ -252,7 +256,8 @@ KV_API int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const
  *    runs were built from; dst_req_offsets/dst_ids the receiver's per-request block
  *    lists (device int32, n_reqs + 1 and any length).  A request whose destination list
  *    is too short sets KV_DERR_DST_TABLE and its uncovered rows are skipped.
- * max_run_blocks: as for kv_pack_blocks.
+ * max_run_blocks, stage_buf: as for kv_pack_blocks (pinned host staging is read over the
+ * host link).
  * stage->n_tensors and n_planes must equal dst's.  Destination ids must be distinct:
  * two staged rows aimed at one destination row race.
  */
@@ -261,6 +266,43 @@ KV_API int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, con
                      int32_t max_run_blocks, const void *stage_buf, int64_t stage_bytes,
                      const int32_t *src_req_offsets, const int32_t *dst_req_offsets,
                      const int32_t *dst_ids, int32_t n_reqs, kv_stream_t stream);
+
+/*
+ * Transfer-completion signal [F section 1.2]: the receiver's per-pair signal counter.
+ * The sender's last put of a transfer adds 1; the receiver waits until the counter reaches
+ * the largest value it expects, which covers every transfer before it.  16 bytes of device
+ * memory, 16-byte aligned, zeroed once by the caller and then only touched by these calls.
+ */
+typedef struct {
+    uint64_t value;    /* monotonic counter */
+    uint32_t arrived;  /* internal: CTAs of the current signalled call that have finished */
+    uint32_t reserved;
+} kv_signal;
+
+/*
+ * kv_unpack_blocks_signal [N section 2.3 step 14, F section 1.2]: kv_unpack_blocks, and once
+ * every row of this call has landed in dst (all tensors), signal->value += add with release
+ * semantics at GPU scope - done by the last CTA of the copy kernel, so no extra launch is
+ * needed (a call with nothing to copy posts the increment with a one-thread kernel).
+ * Signalled calls sharing a signal must be ordered (one stream, or events).
+ */
+KV_API int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
+                                   const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
+                                   int32_t max_run_blocks, const void *stage_buf, int64_t stage_bytes,
+                                   const int32_t *src_req_offsets, const int32_t *dst_req_offsets,
+                                   const int32_t *dst_ids, int32_t n_reqs, kv_signal *signal, uint64_t add,
+                                   kv_stream_t stream);
+
+/*
+ * kv_wait_signal [F section 1.2, flagcxWaitSignal: "GPU 侧 poll signal_buffer >= expected"]:
+ * queues on `stream` a one-thread kernel that polls signal->value (acquire loads) until it
+ * is >= expected, so work queued after it on `stream` starts only then.  The wait is
+ * bounded: after timeout_us microseconds (1 .. 60,000,000; otherwise KV_ERR_RANGE) it gives
+ * up, writes KV_ERR_TIMEOUT to *status_out (device int32, may be NULL) and sets
+ * KV_DERR_TIMEOUT; on success it writes KV_OK.  The context stays usable either way.
+ */
+KV_API int kv_wait_signal(const kv_signal *signal, uint64_t expected, uint32_t timeout_us, int32_t *status_out,
+                          kv_stream_t stream);
 
 /*
  * kv_get_last_error: copies the current device's sticky error word (KV_DERR_* bits) to

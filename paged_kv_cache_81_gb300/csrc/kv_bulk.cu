@@ -243,8 +243,13 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
         }
         __syncwarp();
     }
-    if (lane == 0) pipe.drain();
+    if (lane == 0) {
+        pipe.drain();
+        // the bulk stores were written by the async proxy: order them before the signal
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     __syncwarp();
+    pkv::signal_on_exit(p);
 }
 
 using BulkFn = void (*)(CopyParams);

@@ -86,6 +86,10 @@ int cuda_status(cudaError_t e);
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 inline bool aligned16(int64_t v) { return (v & 15) == 0; }
 
+// Adds `add` to signal->value on `stream` (one thread, release semantics) - used when a
+// signalled call has no copy to make (kv_signal.cu).
+int post_signal(kv_signal *signal, uint64_t add, cudaStream_t s);
+
 // Validates a cache descriptor; checks the tensor base addresses too.
 int check_cache(const kv_cache_desc *c);
 

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_consta
                 if (dst[u] != nullptr) pkv::st_stream(dst[u], v[u]);
         }
     }
+    pkv::signal_on_exit(p);
 }
 
 using KernelFn = void (*)(CopyParams);
@@ -211,6 +212,29 @@ bool bulk_engine(int64_t block_bytes)
     return block_bytes >= 16 * 1024;
 }
 
+// The staging buffer may be device memory or pinned host memory (cudaHostAlloc /
+// cudaHostRegister), the spill target of a receiver whose device memory is short.  Host
+// memory is addressed through its device mapping; unregistered host memory is refused.
+int staging_address(uint8_t *buf, uint8_t **dev_addr, bool *is_host)
+{
+    *is_host = false;
+    *dev_addr = buf;
+    if (buf == nullptr) return KV_OK;
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, buf);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return KV_ERR_INVALID_ARG;
+    }
+    if (a.type == cudaMemoryTypeUnregistered) return KV_ERR_INVALID_ARG;
+    if (a.type == cudaMemoryTypeHost) {
+        if (a.devicePointer == nullptr) return KV_ERR_INVALID_ARG;
+        *is_host = true;
+        *dev_addr = static_cast<uint8_t *>(a.devicePointer);
+    }
+    return KV_OK;
+}
+
 bool block_contiguous(const kv_cache_desc *c, int32_t row_off, int32_t slice)
 {
     return row_off == 0 && slice == c->row_bytes && c->token_stride == c->row_bytes &&
@@ -220,13 +244,17 @@ bool block_contiguous(const kv_cache_desc *c, int32_t row_off, int32_t slice)
 int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, bool pack, int32_t row_off,
            const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity, uint8_t *stage_buf,
            int32_t max_run_blocks, int32_t dst_block_size, const int32_t *src_req_offsets,
-           const int32_t *dst_req_offsets, const int32_t *dst_ids, int32_t n_reqs, cudaStream_t s)
+           const int32_t *dst_req_offsets, const int32_t *dst_ids, int32_t n_reqs, kv_signal *signal,
+           uint64_t signal_add, cudaStream_t s)
 {
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
     const int64_t stage_block_bytes = (int64_t)stage->n_planes * stage->block_size * stage->slice_bytes;
     const int64_t cpb = stage_block_bytes / 16;
     if (cpb >= (1ll << 31)) return KV_ERR_UNSUPPORTED;
+    bool host_stage = false;
+    int st = staging_address(stage_buf, &stage_buf, &host_stage);
+    if (st != KV_OK) return st;
 
     CopyParams p{};
     p.runs = runs;
@@ -255,15 +283,18 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     const int64_t run_chunks = (int64_t)std::max(1, max_run_blocks) * cpb;
     p.max_pieces = max_run_blocks > 0 ? (int32_t)std::min<int64_t>((run_chunks + kPieceChunks - 1) / kPieceChunks, 1 << 20) : 1;
 
-    const bool bulk = (mode == MERGED || mode == BLOCKS) && bulk_engine(stage_block_bytes);
+    // staging in host memory goes over the host link with the warp engine's 16-byte accesses
+    const bool bulk = !host_stage && (mode == MERGED || mode == BLOCKS) && bulk_engine(stage_block_bytes);
     const KernelFn fn = pick(mode, pack);
     const int grid = bulk ? 0 : dev->num_sms * resident_ctas(dev->device, mode, pack);
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
         const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
         p.n_tensors = nt;
         p.tensor_begin = t0;
+        const bool last = t0 + pkv::kMaxTensorsPerLaunch >= cache->n_tensors;
+        p.signal = last ? signal : nullptr;
+        p.signal_add = signal_add;
         for (int32_t t = 0; t < nt; t++) p.base[t] = cache->base[t0 + t];
-        int st;
         if (bulk) {
             st = pkv::launch_bulk_copy(p, mode, pack, *dev, s);
         } else {
@@ -314,15 +345,17 @@ int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const kv_sta
         mode = src->block_stride == blk_bytes ? MERGED : BLOCKS;
     }
     return launch(src, stage, mode, true, src_slice_off, runs, n_runs, run_capacity, (uint8_t *)stage_buf,
-                  max_run_blocks, 0, nullptr, nullptr, nullptr, 0, (cudaStream_t)stream);
+                  max_run_blocks, 0, nullptr, nullptr, nullptr, 0, nullptr, 0, (cudaStream_t)stream);
 }
 
-int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
+int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
                         const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
                         int32_t max_run_blocks, const void *stage_buf, int64_t stage_bytes,
                         const int32_t *src_req_offsets, const int32_t *dst_req_offsets,
-                        const int32_t *dst_ids, int32_t n_reqs, kv_stream_t stream)
+                        const int32_t *dst_ids, int32_t n_reqs, kv_signal *signal, uint64_t add,
+                        kv_stream_t stream)
 {
+    if (signal != nullptr && ((uintptr_t)signal & 15u) != 0) return KV_ERR_ALIGN;
     int st = pkv::check_cache(dst);
     if (st != KV_OK) return st;
     st = check_stage(stage, stage_buf, stage_bytes);
@@ -336,7 +369,8 @@ int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_s
     if (remap && (src_req_offsets == nullptr || dst_req_offsets == nullptr || n_reqs < 0))
         return KV_ERR_INVALID_ARG;
     if (!remap && stage->block_size != dst->block_size) return KV_ERR_INVALID_ARG;
-    if (dst->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0) return KV_OK;
+    if (dst->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0)
+        return signal != nullptr ? pkv::post_signal(signal, add, (cudaStream_t)stream) : KV_OK;
     if (runs == nullptr || n_runs == nullptr) return KV_ERR_INVALID_ARG;
     int mode = REMAP;
     if (!remap) {
@@ -348,7 +382,17 @@ int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_s
     }
     return launch(dst, stage, mode, false, dst_slice_off, runs, n_runs, run_capacity,
                   (uint8_t *)const_cast<void *>(stage_buf), max_run_blocks, dst->block_size, src_req_offsets,
-                  dst_req_offsets, dst_ids, n_reqs, (cudaStream_t)stream);
+                  dst_req_offsets, dst_ids, n_reqs, signal, add, (cudaStream_t)stream);
+}
+
+int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
+                     const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,
+                     int32_t max_run_blocks, const void *stage_buf, int64_t stage_bytes,
+                     const int32_t *src_req_offsets, const int32_t *dst_req_offsets,
+                     const int32_t *dst_ids, int32_t n_reqs, kv_stream_t stream)
+{
+    return kv_unpack_blocks_signal(dst, dst_slice_off, stage, runs, n_runs, run_capacity, max_run_blocks, stage_buf,
+                                   stage_bytes, src_req_offsets, dst_req_offsets, dst_ids, n_reqs, nullptr, 0, stream);
 }
 
 }  // extern "C"

@@ -34,8 +34,30 @@ struct CopyParams {
     const int32_t *dst_ids;
     int32_t n_reqs;
     int *err;
+    kv_signal *signal;    // when set: the last CTA to finish adds signal_add to signal->value
+    uint64_t signal_add;
     uint64_t base[kMaxTensorsPerLaunch];
 };
+
+// End of a copy kernel when a completion signal is requested (every thread of the CTA calls
+// it after its last copy): the CTA's writes are fenced, the CTA is counted on
+// signal->arrived, and the last CTA of the grid resets the count and publishes
+// signal->value += add with release semantics.
+__device__ __forceinline__ void signal_on_exit(const CopyParams &p)
+{
+    if (p.signal == nullptr) return;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomicAdd(&p.signal->arrived, 1u);
+        if (prev == gridDim.x - 1) {
+            p.signal->arrived = 0;
+            __threadfence();
+            asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(&p.signal->value), "l"(p.signal_add)
+                         : "memory");
+        }
+    }
+}
 
 // Launches the TMA bulk-copy engine for a MERGED or BLOCKS copy (kv_bulk.cu).
 int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s);

@@ -25,7 +25,7 @@ KV_DERR_CAPACITY, KV_DERR_STAGE, KV_DERR_DST_TABLE, KV_DERR_TIMEOUT = 0x10, 0x20
 RUN_WORDS = 6  # a kv_xfer_run is 24 bytes: six int32 words (the last two hold the int64 stage_block)
 EXPORTS = ("kv_version", "kv_status_string", "kv_last_cuda_error", "kv_slot_mapping", "kv_reshape_and_cache",
            "kv_xfer_workspace_bytes", "kv_build_xfer_list", "kv_pack_blocks", "kv_unpack_blocks",
-           "kv_get_last_error", "kv_build_xfer_list_static")
+           "kv_get_last_error", "kv_build_xfer_list_static", "kv_unpack_blocks_signal", "kv_wait_signal")
 
 
 class KvError(RuntimeError):
@@ -86,6 +86,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "kv_unpack_blocks": ([D, i32, S, P, P, i64, i32, P, i64, P, P, P, i32, P], ctypes.c_int),
             "kv_get_last_error": ([ctypes.POINTER(i32), i32, P], ctypes.c_int),
             "kv_build_xfer_list_static": ([P, i32, P, P, i64, i32, P, i64, P, P], ctypes.c_int),
+            "kv_unpack_blocks_signal": ([D, i32, S, P, P, i64, i32, P, i64, P, P, P, i32, P, ctypes.c_uint64, P],
+                                        ctypes.c_int),
+            "kv_wait_signal": ([P, ctypes.c_uint64, ctypes.c_uint32, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -117,6 +120,13 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
         return None
     if not t.is_cuda:
         raise ValueError("libpagedkv takes CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stage_ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    """Staging may live in device memory or in pinned host memory (reached over the host link)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("the staging buffer must be a CUDA tensor or pinned host memory")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -293,23 +303,49 @@ def kv_pack_blocks(cache: PagedCache, xfer: XferList, n_blocks: int, stage: Opti
     d = cache.desc()
     _check("kv_pack_blocks", load().kv_pack_blocks(
         ctypes.byref(d), int(slice_off), ctypes.byref(sd), _ptr(xfer.runs), _ptr(xfer.n_runs), xfer.capacity,
-        xfer.max_run_blocks, _ptr(stage), stage.numel() * stage.element_size(), _stream(stream)))
+        xfer.max_run_blocks, _stage_ptr(stage), stage.numel() * stage.element_size(), _stream(stream)))
     return stage
 
 
 def kv_unpack_blocks(cache: PagedCache, stage: torch.Tensor, xfer: XferList, n_blocks: int, src_block_size: int,
                      slice_bytes: Optional[int] = None, dst_slice_off: int = 0,
                      src_req_offsets: Optional[torch.Tensor] = None, dst_req_offsets: Optional[torch.Tensor] = None,
-                     dst_ids: Optional[torch.Tensor] = None, stream=None):
-    """Whole-block mode when dst_ids is None (runs carry destination ids), remap mode otherwise."""
+                     dst_ids: Optional[torch.Tensor] = None, stream=None, signal: Optional[torch.Tensor] = None,
+                     signal_add: int = 1):
+    """Whole-block mode when dst_ids is None (runs carry destination ids), remap mode otherwise.
+    With `signal` (see new_signal) the call is kv_unpack_blocks_signal: signal value += signal_add
+    once every row has landed."""
     sb = cache.row_bytes if slice_bytes is None else int(slice_bytes)
     sd = stage_desc(n_blocks, len(cache.tensors), cache.n_planes, src_block_size, sb)
     n_reqs = 0 if dst_req_offsets is None else dst_req_offsets.shape[0] - 1
     d = cache.desc()
-    _check("kv_unpack_blocks", load().kv_unpack_blocks(
-        ctypes.byref(d), int(dst_slice_off), ctypes.byref(sd), _ptr(xfer.runs), _ptr(xfer.n_runs), xfer.capacity,
-        xfer.max_run_blocks, _ptr(stage), stage.numel() * stage.element_size(), _ptr(src_req_offsets),
-        _ptr(dst_req_offsets), _ptr(dst_ids), n_reqs, _stream(stream)))
+    args = [ctypes.byref(d), int(dst_slice_off), ctypes.byref(sd), _ptr(xfer.runs), _ptr(xfer.n_runs), xfer.capacity,
+            xfer.max_run_blocks, _stage_ptr(stage), stage.numel() * stage.element_size(), _ptr(src_req_offsets),
+            _ptr(dst_req_offsets), _ptr(dst_ids), n_reqs]
+    if signal is None:
+        _check("kv_unpack_blocks", load().kv_unpack_blocks(*args, _stream(stream)))
+    else:
+        _check("kv_unpack_blocks_signal", load().kv_unpack_blocks_signal(*args, _ptr(signal), int(signal_add),
+                                                                         _stream(stream)))
+
+
+def new_signal(device="cuda") -> torch.Tensor:
+    """A zeroed kv_signal (16 bytes: value int64, arrived + reserved) in device memory."""
+    return torch.zeros(2, dtype=torch.int64, device=device)
+
+
+def signal_value(signal: torch.Tensor) -> int:
+    return int(signal[0].item())
+
+
+def kv_wait_signal(signal: torch.Tensor, expected: int, timeout_us: int, status: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """Queue a bounded device-side wait until signal value >= expected; returns the device status word."""
+    if status is None:
+        status = torch.full((1,), -1, dtype=torch.int32, device=signal.device)
+    _check("kv_wait_signal", load().kv_wait_signal(_ptr(signal), int(expected), int(timeout_us), _ptr(status),
+                                                   _stream(stream)))
+    return status
 
 
 def kv_get_last_error(clear: bool = True, stream=None) -> int:

@@ -38,7 +38,7 @@ class StepBytes:
 
 class TransferStep:
     def __init__(self, wl: Workload, case: Case, src_tensors, dst_tensors=None, new_kv=None,
-                 max_run_blocks: Optional[int] = None, device="cuda"):
+                 max_run_blocks: Optional[int] = None, device="cuda", host_stage: bool = False):
         self.wl, self.case = wl, case
         self.device = torch.device(device)
         self.src = K.PagedCache.from_tensors(src_tensors, wl.src.layout)
@@ -68,7 +68,11 @@ class TransferStep:
         self.xfer = K.XferList(n, dev, self.max_run_blocks)
         self.workspace = torch.empty(K.kv_xfer_workspace_bytes(n), dtype=torch.uint8, device=dev)
         sd = K.stage_desc(n, len(self.src.tensors), wl.src.n_planes, wl.src.block_size, self.slice_bytes)
-        self.stage = torch.empty(max(16, K.stage_nbytes(sd)), dtype=torch.uint8, device=dev)
+        # the staging buffer lives in HBM, or in pinned host memory (the receiver's spill target)
+        if host_stage:
+            self.stage = torch.empty(max(16, K.stage_nbytes(sd)), dtype=torch.uint8, pin_memory=True)
+        else:
+            self.stage = torch.empty(max(16, K.stage_nbytes(sd)), dtype=torch.uint8, device=dev)
 
     # -- the five calls ---------------------------------------------------------
     def write_tokens(self, stream=None):
@@ -119,7 +123,6 @@ class TransferStep:
         wl, case = self.wl, self.case
         nt = len(self.src.tensors)
         payload = nt * case.n_blocks * wl.src.n_planes * wl.src.block_size * self.slice_bytes
-        n_runs_words = 24  # per run record written by the builder / read by a copy kernel
         T = self.n_tokens
         slot_b = T * (4 + 4 + 4 + 8) if T else 0  # req, pos, table entry read; slot written
         reshape_b = (nt * wl.src.n_planes * T * wl.src.row_bytes * 2 + T * 8) if T else 0

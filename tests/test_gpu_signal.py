@@ -1,0 +1,110 @@
+"""Completion signals: unpack posts a counter increment once its rows have landed; a
+bounded device-side wait releases the stream when the counter reaches the expected value.
+
+Protocol of the FlagCX connector ("5. flagcx connector design & dev & test", section 1.2):
+the sender adds 1 with the last put of each transfer; the receiver waits for the largest
+expected value.  Every wait here either follows the signalling call on the same stream
+or waits on a counter nothing sets and must time out, reporting KV_ERR_TIMEOUT.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_81_gb300 import pagedkv as K
+from paged_kv_cache_81_gb300 import workloads as W
+from paged_kv_cache_81_gb300.step import TransferStep
+from tests import gpu_support as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_81_gb300 import build
+    build.build()
+    K.load()
+
+
+def _signalled_unpack(step: TransferStep, signal, add):
+    wl = step.wl
+    if step.equal:
+        K.kv_unpack_blocks(step.dst, step.stage, step.xfer, step.case.n_blocks, wl.src.block_size, step.slice_bytes,
+                           wl.dst_slice_off, signal=signal, signal_add=add)
+    else:
+        K.kv_unpack_blocks(step.dst, step.stage, step.xfer, step.case.n_blocks, wl.src.block_size, step.slice_bytes,
+                           wl.dst_slice_off, step.req_offsets, step.dst_req_offsets, step.dst_ids, signal=signal,
+                           signal_add=add)
+
+
+# small page: register-staged engine; small mid: TMA bulk engine; small asym: token remap
+@pytest.mark.parametrize("wl", [W.small(W.PAGE), W.small(W.MID), W.small(W.ASYM)], ids=lambda w: w.name)
+def test_unpack_signal_then_wait(wl):
+    case = W.make_case(wl)
+    src, dst, new = G.host_inputs(wl, case, seed=wl.seed + 55)
+    s_dev, d_dev = W.to_device_bf16(src, "cuda"), W.to_device_bf16(dst, "cuda")
+    n_dev = [x.reshape(G._new_shape(wl.src, case.n_tokens)) for x in W.to_device_bf16(new, "cuda")]
+    K.kv_get_last_error(clear=True)
+    step = TransferStep(wl, case, s_dev, d_dev, n_dev)
+    step.write_tokens()
+    step.build()
+    step.pack()
+    sig = K.new_signal()
+    _signalled_unpack(step, sig, 1)
+    status = K.kv_wait_signal(sig, 1, 1_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == K.KV_OK
+    assert K.signal_value(sig) == 1 and int(sig[1].item()) == 0  # arrival count reset for reuse
+    # two more transfers: the waiter asks for the largest expected value
+    _signalled_unpack(step, sig, 1)
+    _signalled_unpack(step, sig, 2)
+    status = K.kv_wait_signal(sig, 4, 1_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == K.KV_OK and K.signal_value(sig) == 4
+    assert K.kv_get_last_error(clear=True) == 0
+    # the scatter itself is still exact (unpacking the same staging again is idempotent)
+    gpu = dict(err=0, slot=step.slot.cpu().numpy() if case.n_tokens else None, runs=step.xfer.host(),
+               stage=step.stage[:G._stage_len(wl, case)].cpu().numpy(),
+               src=[x.cpu().view(torch.int16).numpy().view(np.uint16) for x in s_dev],
+               dst=[x.cpu().view(torch.int16).numpy().view(np.uint16) for x in d_dev])
+    G.compare(gpu, G.run_oracle(wl, case, src, dst, new, step.max_run_blocks), wl.name + " signalled")
+
+
+def test_wait_times_out_on_a_counter_nothing_sets():
+    K.kv_get_last_error(clear=True)
+    sig = K.new_signal()
+    status = K.kv_wait_signal(sig, 1, 20_000)  # 20 ms
+    torch.cuda.synchronize()
+    assert int(status.item()) == K.KV_ERR_TIMEOUT
+    assert K.kv_get_last_error(clear=True) & K.KV_DERR_TIMEOUT
+    # the context is still usable: a satisfied wait right after succeeds
+    sig[0] = 3
+    status = K.kv_wait_signal(sig, 3, 20_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == K.KV_OK and K.kv_get_last_error() == 0
+
+
+def test_zero_work_unpack_still_signals():
+    g = W.CacheGeom("separate", 8, 4, 1, 64)
+    cache = K.PagedCache.from_tensors(W.device_cache(g, 1, "cuda", seed=5), "separate")
+    off = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ids = torch.zeros(0, dtype=torch.int32, device="cuda")
+    x = K.kv_build_xfer_list(off, ids)
+    stage = torch.empty(16, dtype=torch.uint8, device="cuda")
+    sig = K.new_signal()
+    K.kv_unpack_blocks(cache, stage, x, 0, 4, signal=sig, signal_add=7)
+    torch.cuda.synchronize()
+    assert K.signal_value(sig) == 7
+
+
+def test_wait_argument_checks():
+    sig = K.new_signal()
+    lib = K.load()
+    import ctypes
+    assert lib.kv_wait_signal(K._ptr(sig), 1, 0, None, K._stream()) == K.KV_ERR_RANGE
+    assert lib.kv_wait_signal(K._ptr(sig), 1, 60_000_001, None, K._stream()) == K.KV_ERR_RANGE
+    assert lib.kv_wait_signal(ctypes.c_void_p(sig.data_ptr() + 8), 1, 10, None, K._stream()) == K.KV_ERR_ALIGN
+    assert lib.kv_wait_signal(None, 1, 10, None, K._stream()) == K.KV_ERR_INVALID_ARG
