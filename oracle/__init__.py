@@ -24,7 +24,8 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-__all__ = ["build", "Cache", "slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack"]
+__all__ = ["build", "Cache", "slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack",
+           "clip_block_lists"]
 
 
 def build(force: bool = False, out: str = _LIB, defines=()) -> str:
@@ -59,8 +60,9 @@ def _bind(path: str):
     lib.ora_build_xfer_list.argtypes = [P, i32, P, P, i64, i32, P, P, P, P, P, i64]
     lib.ora_pack.argtypes = [ctypes.POINTER(_OraCache), i32, i32, P, i32, P, i64, P]
     lib.ora_unpack.argtypes = [ctypes.POINTER(_OraCache), i32, i32, i32, i32, P, i32, i64, P, P, i64, P]
+    lib.ora_clip_block_lists.argtypes = [P, i32, P, i64, P, i32, i32, P, P]
     for f in (lib.ora_slot_mapping, lib.ora_reshape_and_cache, lib.ora_build_xfer_list,
-              lib.ora_pack, lib.ora_unpack):
+              lib.ora_pack, lib.ora_unpack, lib.ora_clip_block_lists):
         f.restype = i64
     return lib
 
@@ -176,3 +178,15 @@ def unpack(cache: Cache, stage, req_offsets, dst_req_offsets, dst_ids, src_block
     return int(_get(lib).ora_unpack(ctypes.byref(c), int(dst_slice_off), int(slice_bytes), int(src_block_size),
                                     cache.n_planes, _ptr(off), off.shape[0] - 1, n, _ptr(doff), _ptr(dids),
                                     dids.shape[0], _ptr(stage)))
+
+
+def clip_block_lists(req_offsets, ids, n_tokens, window, block_size, lib=None):
+    """Sliding-window clip of per-request block lists; returns (out_offsets, out_ids)."""
+    off, ids_, nt = _i32(req_offsets), _i32(ids), _i32(n_tokens)
+    out_off = np.zeros(off.shape[0], np.int32)
+    out = np.zeros(max(1, ids_.shape[0]), np.int32)
+    k = _get(lib).ora_clip_block_lists(_ptr(off), off.shape[0] - 1, _ptr(ids_), ids_.shape[0], _ptr(nt), int(window),
+                                       int(block_size), _ptr(out_off), _ptr(out))
+    if k < 0:
+        raise ValueError("oracle clip_block_lists rejected its input")
+    return out_off, out[:k]

@@ -259,3 +259,34 @@ int64_t ora_unpack(const ora_cache *dst, int32_t dst_slice_off, int32_t slice_by
                     }
     return 0;
 }
+
+/* ---- sliding-window clip [M section 3.1] -------------------------------------------
+ * request_finished hands the sender get_sw_clipped_blocks(block_ids); the function's body
+ * is not on the page.  Reading: a layer whose attention sees only the last `window`
+ * tokens needs, of a request with n = n_tokens[r] tokens, only the blocks that hold tokens
+ * max(0, n - window) .. n - 1, i.e. list entries
+ *     q = max(0, n - window) / block_size  ..  ceil(n / block_size) - 1
+ * (never past the request's list).  window <= 0 keeps every block that holds a token.
+ * The kept entries go, in order, to out_ids with CSR out_offsets[n_reqs + 1].
+ * Returns the number of kept entries; -1 if the CSR is inconsistent, block_size <= 0 or
+ * a token count is negative. */
+int64_t ora_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, const int32_t *ids, int64_t n_ids,
+                             const int32_t *n_tokens, int32_t window, int32_t block_size,
+                             int32_t *out_offsets, int32_t *out_ids)
+{
+    if (!csr_ok(req_offsets, n_reqs, n_ids) || block_size <= 0) return -1;
+    int64_t k = 0;
+    out_offsets[0] = 0;
+    for (int32_t r = 0; r < n_reqs; r++) {
+        int64_t n = n_tokens[r];
+        if (n < 0) return -1;
+        int64_t first_token = (window > 0 && n > window) ? n - window : 0;
+        int64_t first = first_token / block_size;
+        int64_t end = (n + block_size - 1) / block_size;
+        int64_t len = req_offsets[r + 1] - req_offsets[r];
+        if (end > len) end = len;
+        for (int64_t q = first; q < end; q++) out_ids[k++] = ids[req_offsets[r] + q];
+        out_offsets[r + 1] = (int32_t)k;
+    }
+    return k;
+}

@@ -1,5 +1,5 @@
-// TMA bulk-copy engine for kv_pack_blocks / kv_unpack_blocks when every block of the cache
-// is one contiguous span (the MERGED and BLOCKS address modes).
+// TMA bulk-copy engine for kv_pack_blocks / kv_unpack_blocks when the cache side is made of
+// contiguous spans: whole runs (MERGED) or one span per (block, plane) (SPANS).
 //
 // Each run of the xfer_list (page "5. flagcx connector design & dev & test", section 1.2:
 // one transfer per contiguous group) becomes one or more bulk copies of at most kStage
@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
     const int64_t g = (int64_t)blockIdx.x * kPipes + w;
     const int64_t P = (int64_t)gridDim.x * kPipes;
     const int64_t block_bytes = p.stage_block_bytes;
+    const int64_t span_bytes = (int64_t)p.div_cps.d * 16;  // one (block, plane) span
 
     kv_xfer_run next{};
     {
@@ -232,11 +233,14 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
                     if (PACK) pipe.span(cache, stage, bytes);
                     else pipe.span(stage, cache, bytes);
                 } else {
+                    const int64_t planes = block_bytes / span_bytes;
                     for (int32_t m = 0; m < run.n_blocks; m++) {
-                        uint8_t *c = cache + (int64_t)m * p.block_stride;
-                        uint8_t *sg = stage + (int64_t)m * block_bytes;
-                        if (PACK) pipe.span(c, sg, block_bytes);
-                        else pipe.span(sg, c, block_bytes);
+                        for (int64_t pl = 0; pl < planes; pl++) {
+                            uint8_t *c = cache + (int64_t)m * p.block_stride + pl * p.plane_stride;
+                            uint8_t *sg = stage + (int64_t)m * block_bytes + pl * span_bytes;
+                            if (PACK) pipe.span(c, sg, span_bytes);
+                            else pipe.span(sg, c, span_bytes);
+                        }
                     }
                 }
             }

@@ -14,8 +14,8 @@
 //
 // Address modes of the cache side (the staging side is always linear):
 //   MERGED  a run is one contiguous span (dense blocks, block_stride == staged block bytes)
-//   BLOCKS  each block is contiguous but blocks are block_stride apart
-//   ROWS    row by row: a head slice, a strided token dimension, or kv-first planes
+//   SPANS   each (block, plane) is contiguous; blocks and planes are strided (kv-first layers)
+//   ROWS    row by row: a head slice or a strided token dimension
 //   REMAP   unpack onto another block size / another block list (token granular)
 #include <algorithm>
 #include <cstdlib>
@@ -29,7 +29,7 @@ namespace {
 using pkv::CopyParams;
 using pkv::FastDiv;
 using pkv::MERGED;
-using pkv::BLOCKS;
+using pkv::SPANS;
 using pkv::ROWS;
 using pkv::REMAP;
 
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_consta
         const uint32_t c_end =
             piece == p.max_pieces - 1 ? item_chunks : (uint32_t)std::min<uint64_t>(c_begin + kPieceChunks, item_chunks);
 
-        int64_t blk = 0;  // first cache block of the run (MERGED / BLOCKS / ROWS)
+        int64_t blk = 0;  // first cache block of the run (MERGED / SPANS / ROWS)
         int32_t j0 = 0, dn = 0;  // REMAP: first staged token of the run in its request; dst list length
         const int32_t *dl = nullptr;
         if (MODE == REMAP) {
@@ -116,10 +116,13 @@ __global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_consta
                 uint8_t *cache_addr;
                 if (MODE == MERGED) {
                     cache_addr = cache_t + blk * p.block_stride + (int64_t)c * 16;
-                } else if (MODE == BLOCKS) {
+                } else if (MODE == SPANS) {
                     const uint32_t m = pkv::fdiv(c, p.div_cpb);
                     const uint32_t w = c - m * p.div_cpb.d;
-                    cache_addr = cache_t + (blk + m) * p.block_stride + (int64_t)w * 16;
+                    const uint32_t plane = pkv::fdiv(w, p.div_cps);
+                    const uint32_t o = w - plane * p.div_cps.d;
+                    cache_addr = cache_t + (blk + m) * p.block_stride + (int64_t)plane * p.plane_stride +
+                                 (int64_t)o * 16;
                 } else {
                     const uint32_t row = pkv::fdiv(c, p.div_cpr);
                     const uint32_t q = c - row * p.div_cpr.d;
@@ -171,8 +174,8 @@ KernelFn pick(int mode, bool pack)
     switch (mode * 2 + (pack ? 1 : 0)) {
     case MERGED * 2 + 1: return copy_runs_kernel<MERGED, true>;
     case MERGED * 2: return copy_runs_kernel<MERGED, false>;
-    case BLOCKS * 2 + 1: return copy_runs_kernel<BLOCKS, true>;
-    case BLOCKS * 2: return copy_runs_kernel<BLOCKS, false>;
+    case SPANS * 2 + 1: return copy_runs_kernel<SPANS, true>;
+    case SPANS * 2: return copy_runs_kernel<SPANS, false>;
     case ROWS * 2 + 1: return copy_runs_kernel<ROWS, true>;
     case ROWS * 2: return copy_runs_kernel<ROWS, false>;
     default: return copy_runs_kernel<REMAP, false>;
@@ -235,10 +238,14 @@ int staging_address(uint8_t *buf, uint8_t **dev_addr, bool *is_host)
     return KV_OK;
 }
 
-bool block_contiguous(const kv_cache_desc *c, int32_t row_off, int32_t slice)
+// Address mode of the cache side: MERGED when a run of blocks is one span, SPANS when every
+// (block, plane) is a span of block_size whole rows, ROWS otherwise.
+int cache_mode(const kv_cache_desc *c, int32_t row_off, int32_t slice)
 {
-    return row_off == 0 && slice == c->row_bytes && c->token_stride == c->row_bytes &&
-           (c->n_planes == 1 || c->plane_stride == (int64_t)c->block_size * c->row_bytes);
+    if (row_off != 0 || slice != c->row_bytes || c->token_stride != c->row_bytes) return ROWS;
+    const int64_t span = (int64_t)c->block_size * c->row_bytes;
+    const bool dense_block = c->n_planes == 1 || c->plane_stride == span;
+    return dense_block && c->block_stride == c->n_planes * span ? MERGED : SPANS;
 }
 
 int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, bool pack, int32_t row_off,
@@ -274,6 +281,7 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     p.div_bs = pkv::make_fastdiv((uint32_t)stage->block_size);
     p.div_rpb = pkv::make_fastdiv((uint32_t)(stage->n_planes * stage->block_size));
     p.div_cpb = pkv::make_fastdiv((uint32_t)cpb);
+    p.div_cps = pkv::make_fastdiv((uint32_t)(cpb / stage->n_planes));
     p.div_dbs = pkv::make_fastdiv((uint32_t)std::max(1, dst_block_size));
     p.src_req_offsets = src_req_offsets;
     p.dst_req_offsets = dst_req_offsets;
@@ -284,7 +292,8 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     p.max_pieces = max_run_blocks > 0 ? (int32_t)std::min<int64_t>((run_chunks + kPieceChunks - 1) / kPieceChunks, 1 << 20) : 1;
 
     // staging in host memory goes over the host link with the warp engine's 16-byte accesses
-    const bool bulk = !host_stage && (mode == MERGED || mode == BLOCKS) && bulk_engine(stage_block_bytes);
+    const int64_t piece = mode == SPANS ? stage_block_bytes / stage->n_planes : stage_block_bytes;
+    const bool bulk = !host_stage && (mode == MERGED || mode == SPANS) && bulk_engine(piece);
     const KernelFn fn = pick(mode, pack);
     const int grid = bulk ? 0 : dev->num_sms * resident_ctas(dev->device, mode, pack);
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
@@ -339,11 +348,7 @@ int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const kv_sta
     if (!pkv::aligned16((int64_t)src_slice_off)) return KV_ERR_ALIGN;
     if (src->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0) return KV_OK;
     if (runs == nullptr || n_runs == nullptr) return KV_ERR_INVALID_ARG;
-    int mode = ROWS;
-    if (block_contiguous(src, src_slice_off, stage->slice_bytes)) {
-        const int64_t blk_bytes = (int64_t)src->n_planes * src->block_size * src->row_bytes;
-        mode = src->block_stride == blk_bytes ? MERGED : BLOCKS;
-    }
+    const int mode = cache_mode(src, src_slice_off, stage->slice_bytes);
     return launch(src, stage, mode, true, src_slice_off, runs, n_runs, run_capacity, (uint8_t *)stage_buf,
                   max_run_blocks, 0, nullptr, nullptr, nullptr, 0, nullptr, 0, (cudaStream_t)stream);
 }
@@ -373,13 +378,7 @@ int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_off, con
         return signal != nullptr ? pkv::post_signal(signal, add, (cudaStream_t)stream) : KV_OK;
     if (runs == nullptr || n_runs == nullptr) return KV_ERR_INVALID_ARG;
     int mode = REMAP;
-    if (!remap) {
-        mode = ROWS;
-        if (block_contiguous(dst, dst_slice_off, stage->slice_bytes)) {
-            const int64_t blk_bytes = (int64_t)dst->n_planes * dst->block_size * dst->row_bytes;
-            mode = dst->block_stride == blk_bytes ? MERGED : BLOCKS;
-        }
-    }
+    if (!remap) mode = cache_mode(dst, dst_slice_off, stage->slice_bytes);
     return launch(dst, stage, mode, false, dst_slice_off, runs, n_runs, run_capacity,
                   (uint8_t *)const_cast<void *>(stage_buf), max_run_blocks, dst->block_size, src_req_offsets,
                   dst_req_offsets, dst_ids, n_reqs, signal, add, (cudaStream_t)stream);

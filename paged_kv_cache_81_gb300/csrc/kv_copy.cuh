@@ -5,7 +5,13 @@
 
 namespace pkv {
 
-enum CopyMode { MERGED = 0, BLOCKS = 1, ROWS = 2, REMAP = 3 };
+// Cache-side address modes of a copy (the staging side is always linear):
+//   MERGED  a run of blocks is one contiguous span
+//   SPANS   every (block, plane) is a contiguous span of block_size rows; blocks and planes are
+//           strided (kv-first layers, padded blocks)
+//   ROWS    row by row: a head slice or a strided token dimension
+//   REMAP   unpack onto another block size / another block list (token granular)
+enum CopyMode { MERGED = 0, SPANS = 1, ROWS = 2, REMAP = 3 };
 
 struct CopyParams {
     const kv_xfer_run *runs;
@@ -28,6 +34,7 @@ struct CopyParams {
     FastDiv div_bs;             // staged (source) block size
     FastDiv div_rpb;            // staged rows per block = planes * bs
     FastDiv div_cpb;            // chunks per staged block
+    FastDiv div_cps;            // chunks per (block, plane) span = bs * slice / 16
     FastDiv div_dbs;            // destination block size (REMAP)
     const int32_t *src_req_offsets;
     const int32_t *dst_req_offsets;
@@ -59,7 +66,7 @@ __device__ __forceinline__ void signal_on_exit(const CopyParams &p)
     }
 }
 
-// Launches the TMA bulk-copy engine for a MERGED or BLOCKS copy (kv_bulk.cu).
+// Launches the TMA bulk-copy engine for a MERGED or SPANS copy (kv_bulk.cu).
 int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s);
 
 }  // namespace pkv

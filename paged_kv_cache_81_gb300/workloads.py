@@ -163,7 +163,12 @@ ASYM = Workload(
     slice_off=4 * 128 * 2, slice_bytes=4 * 128 * 2, dst_slice_off=0,
     spec=_spec(n_reqs=24, len_lo=512, len_hi=8192))
 
-PRESETS = {w.name: w for w in (TINY, MID, PAGE, MLA, ASYM)}
+# The page-shaped cache in the other layer layout of the drawing, (2, num_blocks, bs, H, D)
+# (FlashAttention's kv-first tensors); same seed, so the same block lists as PAGE.
+PAGE_KV_FIRST = replace(PAGE, name="page_shaped_kv_first",
+                        src=CacheGeom("kv_first", 147456, 16, 1, 128), dst=CacheGeom("kv_first", 147456, 16, 1, 128))
+
+PRESETS = {w.name: w for w in (TINY, MID, PAGE, MLA, ASYM, PAGE_KV_FIRST)}
 
 
 def small(wl: Workload) -> Workload:
@@ -176,16 +181,16 @@ def small(wl: Workload) -> Workload:
         return wl
     if wl.kind == "mid":
         g = replace(wl.src, num_blocks=2048)
-        return replace(wl, name="mid_small", n_layers=2, src=g, dst=g).with_spec(n_reqs=5, blocks_per_req=96)
+        return replace(wl, name=wl.name + "_small", n_layers=2, src=g, dst=g).with_spec(n_reqs=5, blocks_per_req=96)
     if wl.kind == "page":
         g = replace(wl.src, num_blocks=4096)
-        return replace(wl, name="page_small", n_layers=3, src=g, dst=g).with_spec(n_reqs=3)
+        return replace(wl, name=wl.name + "_small", n_layers=3, src=g, dst=g).with_spec(n_reqs=3)
     if wl.kind == "mla":
         g = replace(wl.src, num_blocks=1024)
-        return replace(wl, name="mla_small", n_layers=3, src=g, dst=g).with_spec(
+        return replace(wl, name=wl.name + "_small", n_layers=3, src=g, dst=g).with_spec(
             decode_reqs=64, n_reqs=4, len_lo=1024, len_hi=8192, max_pos=8191, table_blocks=128)
     if wl.kind == "asym":
-        return replace(wl, name="asym_small", n_layers=2,
+        return replace(wl, name=wl.name + "_small", n_layers=2,
                        src=replace(wl.src, num_blocks=4096),
                        dst=replace(wl.dst, num_blocks=1024)).with_spec(n_reqs=5)
     raise ValueError(wl.kind)

@@ -75,3 +75,15 @@ def random_cache(geom, n_tensors, seed):
 def random_rows(n_rows, row_bytes, count, seed):
     rng = np.random.default_rng(seed)
     return [rng.integers(0, 256, size=(n_rows, row_bytes), dtype=np.uint8) for _ in range(count)]
+
+
+def read_clip_golden():
+    rows = []
+    for line in open(golden_path("sw_clip_examples.txt"), encoding="utf-8"):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        left, right = line.split(";")
+        a = [int(x) for x in left.split()]
+        rows.append(dict(bs=a[0], window=a[1], n=a[2], ids=a[3:], want=[int(x) for x in right.split()]))
+    return rows

@@ -25,7 +25,7 @@ from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
 
-FULL = [W.MID, W.PAGE, W.MLA, W.ASYM]
+FULL = [W.MID, W.PAGE, W.MLA, W.ASYM, W.PAGE_KV_FIRST]
 
 
 @pytest.fixture(scope="module", autouse=True)

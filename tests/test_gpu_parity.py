@@ -30,7 +30,7 @@ def _lib():
     K.load()
 
 
-PRESETS = [W.TINY, W.small(W.MID), W.small(W.PAGE), W.small(W.MLA), W.small(W.ASYM)]
+PRESETS = [W.TINY, W.small(W.MID), W.small(W.PAGE), W.small(W.MLA), W.small(W.ASYM), W.small(W.PAGE_KV_FIRST)]
 
 
 @pytest.mark.parametrize("wl", PRESETS, ids=lambda w: w.name)

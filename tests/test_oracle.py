@@ -266,9 +266,44 @@ def pin_xfer_random(lib):
         assert rows == want
 
 
+def pin_clip_golden(lib):
+    for c in H.read_clip_golden():
+        off, ids = W.csr([c["ids"]])
+        o, got = oracle.clip_block_lists(off, ids, [c["n"]], c["window"], c["bs"], lib=lib)
+        assert got.tolist() == c["want"], c
+        assert o.tolist() == [0, len(c["want"])]
+
+
+def pin_clip_brute(lib):
+    """The blocks holding the last `window` tokens, found by enumerating block filling."""
+    rng = np.random.default_rng(91)
+    for trial in range(60):
+        bs = int(rng.choice([1, 2, 3, 16]))
+        R = int(rng.integers(1, 6))
+        lens = rng.integers(0, 9, size=R)
+        perm = rng.permutation(200)
+        lists = W.pop_lists(perm, lens)
+        n_tok = [int(rng.integers(0, l * bs + 1)) for l in lens]
+        window = int(rng.choice([0, 1, 3, 5, 17, 1000]))
+        off, ids = W.csr(lists)
+        o, got = oracle.clip_block_lists(off, ids, n_tok, window, bs, lib=lib)
+        want = []
+        for l, n in zip(lists, n_tok):
+            slots = brute.token_slots(l, n, 200, bs)
+            first = max(0, n - window) if window > 0 else 0
+            seen = []
+            for s_ in slots[first:]:
+                b = int(np.unravel_index(s_, (200, bs))[0])
+                if b not in seen:
+                    seen.append(b)
+            want.extend(seen)
+        assert got.tolist() == want, (bs, window, n_tok, lists)
+        assert o[-1] == len(want)
+
+
 PINS = [pin_slot_golden, pin_slot_brute, pin_reshape_indexing, pin_pack_indexing, pin_pack_brute,
         pin_unpack_roundtrip, pin_unpack_other_ids, pin_unpack_remap_handworked, pin_unpack_brute,
-        pin_xfer_golden, pin_xfer_random]
+        pin_xfer_golden, pin_xfer_random, pin_clip_golden, pin_clip_brute]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -386,6 +421,9 @@ MUTANTS = [
     ("unpack uses src block size for dst slot", "j % dst->block_size) + dst_slice_off", "j % src_block_size) + dst_slice_off"),
     ("unpack wrong dst block index", "dst_ids[dst_req_offsets[r] + j / dst->block_size]", "dst_ids[dst_req_offsets[r] + q]"),
     ("unpack ignores dst slice offset", ") + dst_slice_off,\n", "),\n"),
+    ("clip keeps one token too many", "? n - window : 0;", "? n - window - 1 : 0;"),
+    ("clip drops the partial last block", "int64_t end = (n + block_size - 1) / block_size;", "int64_t end = n / block_size;"),
+    ("clip ignores the window", "int64_t first = first_token / block_size;", "int64_t first = 0;"),
 ]
 
 
