@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     ap.add_argument("--stage", default="device", choices=["device", "host"],
                     help="staging buffer in HBM, or in pinned host memory (pack/unpack over the host link)")
+    ap.add_argument("--sw-window", type=int, default=0,
+                    help="clip every request's block lists to the last N tokens before the xfer_list (0 = off)")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling captures)")
     ap.add_argument("--num-blocks", type=int, default=None, help="override blocks per tensor (profiling captures)")
     return ap.parse_args()
@@ -193,6 +195,8 @@ def config_dict(wl: W.Workload, case: W.Case, step=None) -> dict:
         d.update(dst_block_size=wl.dst.block_size, slice_bytes=wl.moved_slice, slice_off=wl.slice_off)
     if step is not None:
         d["max_run_blocks"] = step.max_run_blocks
+        if step.sw_window:
+            d.update(sw_window=step.sw_window, blocks_sent=step.n_listed)
     return d
 
 
@@ -222,7 +226,8 @@ def run_ours(args):
     src = W.device_cache(wl.src, wl.n_tensors, dev, seed=seed)
     dst = W.device_cache(wl.dst, wl.n_tensors, dev, seed=seed + 1) if wl.kind != "mla" else None
     new = W.new_token_rows(wl.src, wl.n_tensors, case.n_tokens, dev, seed=seed + 2)
-    step = TransferStep(wl, case, src, dst, new, device=dev, host_stage=args.stage == "host")
+    step = TransferStep(wl, case, src, dst, new, device=dev, host_stage=args.stage == "host",
+                        sw_window=args.sw_window or None)
     stream = torch.cuda.current_stream(dev)
     K.kv_get_last_error(clear=True)
 

@@ -222,6 +222,25 @@ KV_API int kv_build_xfer_list_static(const int32_t *req_offsets, int32_t n_reqs,
                                      kv_stream_t stream);
 
 /*
+ * kv_clip_block_lists [M section 3.1: request_finished sends get_sw_clipped_blocks(block_ids)]:
+ * the sliding-window clip of per-request block lists, applied before kv_build_xfer_list.  The
+ * function's body is not on the page; reading: a layer attending to the last `window` tokens
+ * needs, of request r with n_tokens[r] tokens, only its list entries
+ *     q = max(0, n_tokens[r] - window) / block_size  ..  ceil(n_tokens[r] / block_size) - 1
+ * (never past the request's list); window <= 0 keeps every entry that holds a token.
+ * req_offsets (n_reqs + 1), ids (n_ids), n_tokens (n_reqs): device int32.  Writes the kept
+ * entries, in order, to out_ids (device, out_capacity >= n_ids) with CSR out_offsets
+ * (device int32, n_reqs + 1).  The kept count is out_offsets[n_reqs]; a caller that knows
+ * n_tokens and the list lengths on the host can compute it without reading the device.
+ * Clip a destination list that is aligned entry-by-entry with the source list with the same
+ * arguments to keep the two aligned.  Inconsistent offsets or negative token counts set
+ * KV_DERR_LIST; no write ever leaves out_ids.  Limit: n_ids < 2^31.
+ */
+KV_API int kv_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, const int32_t *ids, int64_t n_ids,
+                               const int32_t *n_tokens, int32_t window, int32_t block_size,
+                               int32_t *out_offsets, int32_t *out_ids, int64_t out_capacity, kv_stream_t stream);
+
+/*
  * kv_pack_blocks [N section 2.4 extract_kv_from_layer, F section 1.2]: for every
  * tensor t and run of `runs`, copies rows (t, src_block + m, p, o) - byte slice
  * [src_slice_off, src_slice_off + stage->slice_bytes) of each row - to the staging

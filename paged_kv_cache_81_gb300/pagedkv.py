@@ -25,7 +25,8 @@ KV_DERR_CAPACITY, KV_DERR_STAGE, KV_DERR_DST_TABLE, KV_DERR_TIMEOUT = 0x10, 0x20
 RUN_WORDS = 6  # a kv_xfer_run is 24 bytes: six int32 words (the last two hold the int64 stage_block)
 EXPORTS = ("kv_version", "kv_status_string", "kv_last_cuda_error", "kv_slot_mapping", "kv_reshape_and_cache",
            "kv_xfer_workspace_bytes", "kv_build_xfer_list", "kv_pack_blocks", "kv_unpack_blocks",
-           "kv_get_last_error", "kv_build_xfer_list_static", "kv_unpack_blocks_signal", "kv_wait_signal")
+           "kv_get_last_error", "kv_build_xfer_list_static", "kv_unpack_blocks_signal", "kv_wait_signal",
+           "kv_clip_block_lists")
 
 
 class KvError(RuntimeError):
@@ -89,6 +90,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "kv_unpack_blocks_signal": ([D, i32, S, P, P, i64, i32, P, i64, P, P, P, i32, P, ctypes.c_uint64, P],
                                         ctypes.c_int),
             "kv_wait_signal": ([P, ctypes.c_uint64, ctypes.c_uint32, P, P], ctypes.c_int),
+            "kv_clip_block_lists": ([P, i32, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -271,6 +273,22 @@ def kv_build_xfer_list(req_offsets: torch.Tensor, src_ids: torch.Tensor, dst_ids
         _ptr(out.runs), out.capacity, _ptr(out.n_runs), _ptr(workspace), workspace.numel(), _stream(stream)))
     out.max_run_blocks = int(max_run_blocks)
     return out
+
+
+def kv_clip_block_lists(req_offsets: torch.Tensor, ids: torch.Tensor, n_tokens: torch.Tensor, window: int,
+                        block_size: int, out_offsets: Optional[torch.Tensor] = None,
+                        out_ids: Optional[torch.Tensor] = None, stream=None):
+    """Sliding-window clip of per-request block lists; returns device (out_offsets, out_ids)
+    where out_ids has room for every input entry and out_offsets[-1] is the kept count."""
+    _i32(req_offsets, "req_offsets"), _i32(ids, "ids"), _i32(n_tokens, "n_tokens")
+    if out_offsets is None:
+        out_offsets = torch.empty_like(req_offsets)
+    if out_ids is None:
+        out_ids = torch.empty(max(1, ids.shape[0]), dtype=torch.int32, device=ids.device)
+    _check("kv_clip_block_lists", load().kv_clip_block_lists(
+        _ptr(req_offsets), req_offsets.shape[0] - 1, _ptr(ids), ids.shape[0], _ptr(n_tokens), int(window),
+        int(block_size), _ptr(out_offsets), _ptr(out_ids), out_ids.shape[0], _stream(stream)))
+    return out_offsets, out_ids
 
 
 KV_XFER_STATIC_MAX_BLOCKS = 4177920

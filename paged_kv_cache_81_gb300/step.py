@@ -4,6 +4,7 @@ A step runs, on one CUDA stream:
   1. kv_slot_mapping        new tokens' slots from the shared block table (when the batch has new tokens)
   2. kv_reshape_and_cache   their K/V rows into every layer's paged tensor
   3. kv_build_xfer_list     the send side's per-request block lists -> contiguous runs
+                            (optionally after kv_clip_block_lists, the sliding-window clip)
   4. kv_pack_blocks         those runs of every tensor -> the staging buffer
   5. kv_unpack_blocks       the staging buffer -> the receiver's cache (whole blocks, or
                             token-granular onto another block size / head slice)
@@ -38,7 +39,8 @@ class StepBytes:
 
 class TransferStep:
     def __init__(self, wl: Workload, case: Case, src_tensors, dst_tensors=None, new_kv=None,
-                 max_run_blocks: Optional[int] = None, device="cuda", host_stage: bool = False):
+                 max_run_blocks: Optional[int] = None, device="cuda", host_stage: bool = False,
+                 sw_window: Optional[int] = None):
         self.wl, self.case = wl, case
         self.device = torch.device(device)
         self.src = K.PagedCache.from_tensors(src_tensors, wl.src.layout)
@@ -65,6 +67,17 @@ class TransferStep:
         stage_block = wl.src.n_planes * wl.src.block_size * self.slice_bytes
         self.max_run_blocks = K.default_max_run_blocks(stage_block) if max_run_blocks is None else max_run_blocks
         n = case.n_blocks
+        self.sw_window = sw_window
+        if sw_window:
+            if not self.equal:
+                raise ValueError("the sliding-window clip keeps source and destination lists aligned entry by entry;"
+                                 " it needs equal geometry")
+            self.req_tokens = t(case.req_tokens)
+            self.clip_offsets = torch.empty_like(self.req_offsets)
+            self.clip_src = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+            self.clip_dst = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+            n = self.kept_blocks(case, sw_window, wl.src.block_size)
+        self.n_listed = n
         self.xfer = K.XferList(n, dev, self.max_run_blocks)
         self.workspace = torch.empty(K.kv_xfer_workspace_bytes(n), dtype=torch.uint8, device=dev)
         sd = K.stage_desc(n, len(self.src.tensors), wl.src.n_planes, wl.src.block_size, self.slice_bytes)
@@ -81,23 +94,44 @@ class TransferStep:
         K.kv_slot_mapping(self.block_table, self.token_req, self.token_pos, self.src.block_size, self.slot, stream)
         K.kv_reshape_and_cache(self.src, self.new_kv, self.slot, stream)
 
+    @staticmethod
+    def kept_blocks(case: Case, window: int, block_size: int) -> int:
+        """Entries the sliding-window clip keeps, from the host's copy of the per-request
+        token counts and list lengths (sizes the staging buffer without a device read)."""
+        kept = 0
+        for r in range(case.n_reqs):
+            n = int(case.req_tokens[r])
+            length = int(case.req_offsets[r + 1] - case.req_offsets[r])
+            end = min(-(-n // block_size), length)
+            first = min((max(0, n - window) if window > 0 else 0) // block_size, end)
+            kept += end - first
+        return kept
+
     def build(self, stream=None):
-        dst = self.dst_ids if (self.equal and self.dst is not None) else None
-        K.kv_build_xfer_list(self.req_offsets, self.src_ids, dst, self.max_run_blocks, self.xfer, self.workspace,
-                             stream)
+        use_dst = self.equal and self.dst is not None
+        offsets, src, dst = self.req_offsets, self.src_ids, self.dst_ids if use_dst else None
+        if self.sw_window:
+            bs = self.wl.src.block_size
+            K.kv_clip_block_lists(self.req_offsets, self.src_ids, self.req_tokens, self.sw_window, bs,
+                                  self.clip_offsets, self.clip_src, stream)
+            if use_dst:
+                K.kv_clip_block_lists(self.req_offsets, self.dst_ids, self.req_tokens, self.sw_window, bs,
+                                      self.clip_offsets, self.clip_dst, stream)
+            offsets, src = self.clip_offsets, self.clip_src[:self.n_listed]
+            dst = self.clip_dst[:self.n_listed] if use_dst else None
+        K.kv_build_xfer_list(offsets, src, dst, self.max_run_blocks, self.xfer, self.workspace, stream)
 
     def pack(self, stream=None):
-        K.kv_pack_blocks(self.src, self.xfer, self.case.n_blocks, self.stage, self.slice_off, self.slice_bytes,
-                         stream)
+        K.kv_pack_blocks(self.src, self.xfer, self.n_listed, self.stage, self.slice_off, self.slice_bytes, stream)
 
     def unpack(self, stream=None):
         if self.dst is None:
             return
         if self.equal:
-            K.kv_unpack_blocks(self.dst, self.stage, self.xfer, self.case.n_blocks, self.wl.src.block_size,
+            K.kv_unpack_blocks(self.dst, self.stage, self.xfer, self.n_listed, self.wl.src.block_size,
                                self.slice_bytes, self.wl.dst_slice_off, stream=stream)
         else:
-            K.kv_unpack_blocks(self.dst, self.stage, self.xfer, self.case.n_blocks, self.wl.src.block_size,
+            K.kv_unpack_blocks(self.dst, self.stage, self.xfer, self.n_listed, self.wl.src.block_size,
                                self.slice_bytes, self.wl.dst_slice_off, self.req_offsets, self.dst_req_offsets,
                                self.dst_ids, stream=stream)
 
@@ -112,6 +146,8 @@ class TransferStep:
         """Kernels of libpagedkv one run() launches (one launch per 128 tensors for the copies)."""
         groups = -(-len(self.src.tensors) // 128)
         n = 1 + groups  # builder + pack
+        if self.sw_window:
+            n += 2 * (2 if (self.equal and self.dst is not None) else 1)  # clip: count + copy per list
         if self.n_tokens:
             n += 1 + groups
         if self.dst is not None:
@@ -122,9 +158,12 @@ class TransferStep:
     def bytes(self) -> StepBytes:
         wl, case = self.wl, self.case
         nt = len(self.src.tensors)
-        payload = nt * case.n_blocks * wl.src.n_planes * wl.src.block_size * self.slice_bytes
+        payload = nt * self.n_listed * wl.src.n_planes * wl.src.block_size * self.slice_bytes
         T = self.n_tokens
         slot_b = T * (4 + 4 + 4 + 8) if T else 0  # req, pos, table entry read; slot written
         reshape_b = (nt * wl.src.n_planes * T * wl.src.row_bytes * 2 + T * 8) if T else 0
-        build_b = case.n_blocks * 4 * (2 if (self.equal and self.dst is not None) else 1)
+        lists = 2 if (self.equal and self.dst is not None) else 1
+        build_b = self.n_listed * 4 * lists
+        if self.sw_window:  # the clip reads every entry and writes the kept ones, per list
+            build_b += (case.n_blocks + self.n_listed) * 4 * lists
         return StepBytes(slot_b, reshape_b, build_b, 2 * payload, 2 * payload if self.dst is not None else 0)

@@ -211,6 +211,7 @@ class Case:
     block_table: Optional[np.ndarray] = None  # int32 [Rw, M]
     token_req: Optional[np.ndarray] = None  # int32 [T]
     token_pos: Optional[np.ndarray] = None  # int32 [T]
+    req_tokens: Optional[np.ndarray] = None  # int32 [R]: tokens each transferred request holds
     info: dict = field(default_factory=dict)
 
     @property
@@ -300,7 +301,7 @@ def _tiny(wl, rng):
     token_req = np.repeat(np.arange(n, dtype=np.int32), new)
     token_pos = np.concatenate([np.arange(l, l + new, dtype=np.int32) for l in lens])
     return Case(wl, off, ids, doff, dids, _table(src_lists), token_req, token_pos,
-                info=dict(lens=lens.tolist()))
+                req_tokens=(lens + new).astype(np.int32), info=dict(lens=lens.tolist()))
 
 
 def _mid(wl, rng):
@@ -310,7 +311,7 @@ def _mid(wl, rng):
     q_dst = fragmented_queue(rng, wl.dst.num_blocks, wl.p("max_piece"), wl.p("keep_prob"))
     off, ids = csr(pop_lists(q_src, [per] * n))
     doff, dids = csr(pop_lists(q_dst, [per] * n))
-    return Case(wl, off, ids, doff, dids)
+    return Case(wl, off, ids, doff, dids, req_tokens=np.full(n, per * wl.src.block_size, np.int32))
 
 
 def _page(wl, rng):
@@ -325,7 +326,8 @@ def _page(wl, rng):
     tok = per * bs
     token_req = np.repeat(np.arange(n, dtype=np.int32), tok)
     token_pos = np.tile(np.arange(tok, dtype=np.int32), n)
-    return Case(wl, off, ids, doff, dids, _table(src_lists), token_req, token_pos)
+    return Case(wl, off, ids, doff, dids, _table(src_lists), token_req, token_pos,
+                req_tokens=np.full(n, tok, np.int32))
 
 
 def _mla(wl, rng):
@@ -343,7 +345,7 @@ def _mla(wl, rng):
     counts = [blocks_for(l, bs) for l in lens]
     off, ids = csr(pop_lists(q, counts, wrap=True))
     return Case(wl, off, ids, off.copy(), ids.copy(), table,
-                np.arange(dn, dtype=np.int32), pos, info=dict(lens=lens.tolist()))
+                np.arange(dn, dtype=np.int32), pos, req_tokens=lens.astype(np.int32), info=dict(lens=lens.tolist()))
 
 
 def _asym(wl, rng):
@@ -353,7 +355,7 @@ def _asym(wl, rng):
     dc = [blocks_for(l, wl.dst.block_size) for l in lens]
     off, ids = csr(pop_lists(rng.permutation(wl.src.num_blocks).astype(np.int32), sc))
     doff, dids = csr(pop_lists(rng.permutation(wl.dst.num_blocks).astype(np.int32), dc))
-    return Case(wl, off, ids, doff, dids, info=dict(lens=lens.tolist()))
+    return Case(wl, off, ids, doff, dids, req_tokens=lens.astype(np.int32), info=dict(lens=lens.tolist()))
 
 
 # --- cache and token contents ----------------------------------------------
