@@ -286,3 +286,42 @@ def test_host_argument_errors():
     assert e.value.status == K.KV_ERR_RANGE
     torch.cuda.synchronize()
     assert K.kv_get_last_error() == 0
+
+
+@pytest.mark.parametrize("layout", ["separate", "blocks_first"])
+def test_more_tensors_than_one_launch_carries(layout):
+    """130 and 257 cache tensors: reshape_and_cache, pack and unpack split into several launches
+    (128 tensor bases per launch); the staging offsets of later launches must continue."""
+    for n_tensors in (130, 257):
+        g = W.CacheGeom(layout, 24, 4, 1, 16)  # 32-byte rows, tiny tensors
+        rng = np.random.default_rng(n_tensors)
+        src = W.host_cache_tensors(g, n_tensors, rng)
+        dst = W.host_cache_tensors(g, n_tensors, rng)
+        lists = [rng.permutation(24)[:5], rng.permutation(24)[:3]]
+        off, ids = W.csr(lists)
+        dids = rng.permutation(24)[:8].astype(np.int32)  # distinct destination blocks
+        T = 6
+        slot = rng.choice(24 * 4, size=T, replace=False).astype(np.int64)
+        new = [rng.integers(-2 ** 15, 2 ** 15, size=(T, 16), dtype=np.int16) for _ in range(n_tensors * g.n_planes)]
+        s_dev, d_dev = W.to_device_bf16(src, "cuda"), W.to_device_bf16(dst, "cuda")
+        scache = K.PagedCache.from_tensors(s_dev, layout)
+        dcache = K.PagedCache.from_tensors(d_dev, layout)
+        n_dev = [torch.from_numpy(x).cuda().view(torch.bfloat16).reshape(T, 1, 16) for x in new]
+        K.kv_reshape_and_cache(scache, n_dev, torch.from_numpy(slot).cuda())
+        t = lambda a: torch.from_numpy(a).cuda()
+        x = K.kv_build_xfer_list(t(off), t(ids), t(dids), 2)
+        stage = K.kv_pack_blocks(scache, x, ids.shape[0])
+        K.kv_unpack_blocks(dcache, stage, x, ids.shape[0], 4)
+        torch.cuda.synchronize()
+        assert K.kv_get_last_error() == 0
+        sh = [a.copy() for a in src]
+        sc = H.ora_cache(g, sh)
+        assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], slot) == 0
+        want = oracle.pack(sc, off, ids)
+        np.testing.assert_array_equal(stage.cpu().numpy(), want)
+        dh = [a.copy() for a in dst]
+        assert oracle.unpack(H.ora_cache(g, dh), want, off, off, dids, 4, g.row_bytes) == 0
+        for a, b in zip(s_dev, sh):
+            np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+        for a, b in zip(d_dev, dh):
+            np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
