@@ -308,6 +308,8 @@ def run_ours(args):
     if step.n_tokens:
         kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
 
+    write_path = measure_write_path(step, dev) if step.n_tokens else None
+
     host_link = None
     if args.stage == "host":
         # the bound of pack/unpack with host staging: device<->pinned copies of the staging size
@@ -339,6 +341,8 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
     }
+    if write_path is not None:
+        line["write_path"] = write_path
     if host_link is not None:
         line["host_link"] = host_link
         line["config"]["stage"] = "pinned host memory"
@@ -348,6 +352,29 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_write_path(step, dev, iters: int = 200) -> dict:
+    """Wall-clock cost of the new-token write (kv_slot_mapping + kv_reshape_and_cache) issued
+    call by call from Python, and replayed from a CUDA graph of the same two calls."""
+    import torch
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(iters):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / iters * 1e6
+
+    eager = timed(step.write_tokens)
+    graph = step.capture(step.write_tokens)
+    replay = timed(graph.replay)
+    del graph
+    return {"tokens": step.n_tokens, "tensors": len(step.src.tensors), "eager_us_per_step": round(eager, 2),
+            "graph_us_per_step": round(replay, 2)}
 
 
 def measure_host_link(host_buf, dev, stream, reps: int = 5) -> dict:

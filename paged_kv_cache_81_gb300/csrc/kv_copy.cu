@@ -33,12 +33,19 @@ using pkv::SPANS;
 using pkv::ROWS;
 using pkv::REMAP;
 
+#ifndef PKV_COPY_UNROLL
+#define PKV_COPY_UNROLL 8  // 16-byte loads each lane keeps in flight
+#endif
+#ifndef PKV_COPY_MIN_CTAS
+#define PKV_COPY_MIN_CTAS 1  // launch-bounds hint: resident CTAs per SM the register budget must allow
+#endif
+
 constexpr int kThreads = 256;
-constexpr int kUnroll = 8;
+constexpr int kUnroll = PKV_COPY_UNROLL;
 constexpr uint32_t kPieceChunks = 1024;  // 16 KiB
 
 template <int MODE, bool PACK>
-__global__ void __launch_bounds__(kThreads) copy_runs_kernel(const __grid_constant__ CopyParams p)
+__global__ void __launch_bounds__(kThreads, PKV_COPY_MIN_CTAS) copy_runs_kernel(const __grid_constant__ CopyParams p)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;

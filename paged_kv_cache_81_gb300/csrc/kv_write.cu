@@ -56,7 +56,10 @@ struct ReshapeParams {
     uint64_t src[pkv::kMaxTensorsPerLaunch * 2];
 };
 
-constexpr int kReshapeUnroll = 4;
+#ifndef PKV_RESHAPE_UNROLL
+#define PKV_RESHAPE_UNROLL 4  // 16-byte loads each thread keeps in flight
+#endif
+constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
 
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p)
 {

@@ -141,6 +141,21 @@ class TransferStep:
         self.pack(stream)
         self.unpack(stream)
 
+    def capture(self, fn=None, stream=None) -> "torch.cuda.CUDAGraph":
+        """Capture run() (or another method of this step, e.g. write_tokens) into a CUDA graph for
+        replay - the way to issue launch-bound steps such as a decode write.
+
+        Run the step once eagerly first: the first call of each entry point on a device looks up
+        per-device state, which must not happen during a capture.  A replay repeats the same
+        five calls on the same buffers; refresh the input tensors in place between replays."""
+        g = torch.cuda.CUDAGraph()
+        s = stream if stream is not None else torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.graph(g, stream=s):
+            (fn or self.run)()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        return g
+
     @property
     def launches_per_step(self) -> int:
         """Kernels of libpagedkv one run() launches (one launch per 128 tensors for the copies)."""
