@@ -309,6 +309,7 @@ def run_ours(args):
         kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
 
     write_path = measure_write_path(step, dev) if step.n_tokens else None
+    prior_art = measure_prior_art(step, dev, stream) if args.stage == "device" and not args.sw_window else None
 
     host_link = None
     if args.stage == "host":
@@ -343,6 +344,8 @@ def run_ours(args):
     }
     if write_path is not None:
         line["write_path"] = write_path
+    if prior_art is not None:
+        line["prior_art"] = prior_art
     if host_link is not None:
         line["host_link"] = host_link
         line["config"]["stage"] = "pinned host memory"
@@ -352,6 +355,60 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_prior_art(step, dev, stream, reps: int = 5):
+    """The pages' own mechanism on the same GPU, for context: the NCCL connector gathers one
+    tensor per (request, layer) with torch advanced indexing, layer[block_ids] (layer[:, block_ids]
+    for kv-first), and the receiver scatters it with layer[block_ids] = tensor.  Whole-row
+    workloads only (no head slice, same block size)."""
+    import torch
+
+    wl, case = step.wl, step.case
+    if wl.moved_slice != wl.src.row_bytes or (step.dst is not None and not step.equal):
+        return None
+    kv_first = wl.src.layout == "kv_first"
+    src_lists = [torch.from_numpy(case.src_ids[case.req_offsets[r]:case.req_offsets[r + 1]].astype("int64")).to(dev)
+                 for r in range(case.n_reqs)]
+    dst_lists = [torch.from_numpy(case.dst_ids[case.dst_req_offsets[r]:case.dst_req_offsets[r + 1]].astype("int64"))
+                 .to(dev) for r in range(case.n_reqs)]
+
+    def gather():
+        return [[(layer[:, ids] if kv_first else layer[ids]) for ids in src_lists] for layer in step.src.tensors]
+
+    def scatter(parts):
+        for layer, per_req in zip(step.dst.tensors, parts):
+            for ids, t in zip(dst_lists, per_req):
+                if kv_first:
+                    layer[:, ids] = t
+                else:
+                    layer[ids] = t
+
+    parts = gather()
+    if step.dst is not None:
+        scatter(parts)
+    torch.cuda.synchronize(dev)
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    g_ms = s_ms = 0.0
+    for _ in range(reps):
+        parts = None  # free the previous gather first (MLA's per-request tensors total ~38 GB)
+        a.record(stream)
+        parts = gather()
+        b.record(stream)
+        if step.dst is not None:
+            scatter(parts)
+        c.record(stream)
+        torch.cuda.synchronize(dev)
+        g_ms += a.elapsed_time(b)
+        s_ms += b.elapsed_time(c)
+    payload = step.bytes().pack  # read + written, as for kv_pack_blocks
+    out = {"kind": "torch advanced indexing per (request, layer): layer[block_ids] gather, "
+                   "layer[block_ids] = tensor scatter",
+           "torch_calls_per_step": len(step.src.tensors) * case.n_reqs * (2 if step.dst is not None else 1),
+           "gather_gbs": round(payload / (g_ms / reps * 1e-3) / 1e9, 1)}
+    if step.dst is not None:
+        out["scatter_gbs"] = round(payload / (s_ms / reps * 1e-3) / 1e9, 1)
+    return out
 
 
 def measure_write_path(step, dev, iters: int = 200) -> dict:
