@@ -25,7 +25,7 @@ _lock = threading.Lock()
 _lib = None
 
 __all__ = ["build", "Cache", "slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack",
-           "clip_block_lists"]
+           "clip_block_lists", "fnv1a64", "block_hashes"]
 
 
 def build(force: bool = False, out: str = _LIB, defines=()) -> str:
@@ -61,8 +61,11 @@ def _bind(path: str):
     lib.ora_pack.argtypes = [ctypes.POINTER(_OraCache), i32, i32, P, i32, P, i64, P]
     lib.ora_unpack.argtypes = [ctypes.POINTER(_OraCache), i32, i32, i32, i32, P, i32, i64, P, P, i64, P]
     lib.ora_clip_block_lists.argtypes = [P, i32, P, i64, P, i32, i32, P, P]
+    lib.ora_fnv1a64.argtypes = [P, i64]
+    lib.ora_fnv1a64.restype = ctypes.c_uint64
+    lib.ora_block_hashes.argtypes = [P, i32, P, i64, i32, ctypes.c_uint64, P, P]
     for f in (lib.ora_slot_mapping, lib.ora_reshape_and_cache, lib.ora_build_xfer_list,
-              lib.ora_pack, lib.ora_unpack, lib.ora_clip_block_lists):
+              lib.ora_pack, lib.ora_unpack, lib.ora_clip_block_lists, lib.ora_block_hashes):
         f.restype = i64
     return lib
 
@@ -189,4 +192,23 @@ def clip_block_lists(req_offsets, ids, n_tokens, window, block_size, lib=None):
                                        int(block_size), _ptr(out_off), _ptr(out))
     if k < 0:
         raise ValueError("oracle clip_block_lists rejected its input")
+    return out_off, out[:k]
+
+
+def fnv1a64(data: bytes, lib=None) -> int:
+    """FNV-1a 64 of a byte string (the hash of the prefix chain)."""
+    buf = np.frombuffer(bytes(data) or b"\0", dtype=np.uint8).copy()
+    return int(_get(lib).ora_fnv1a64(_ptr(buf), len(data)))
+
+
+def block_hashes(tok_offsets, tokens, block_size, seed, lib=None):
+    """Prefix hash chain of every request's full blocks; returns (out_offsets int32, hashes uint64)."""
+    off, tok = _i32(tok_offsets), _i32(tokens)
+    n_full = sum(int(off[r + 1] - off[r]) // int(block_size) for r in range(off.shape[0] - 1))
+    out_off = np.zeros(off.shape[0], np.int32)
+    out = np.zeros(max(1, n_full), np.uint64)
+    k = _get(lib).ora_block_hashes(_ptr(off), off.shape[0] - 1, _ptr(tok), tok.shape[0], int(block_size),
+                                   int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_off), _ptr(out))
+    if k < 0:
+        raise ValueError("oracle block_hashes rejected its input")
     return out_off, out[:k]

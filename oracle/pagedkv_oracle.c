@@ -290,3 +290,49 @@ int64_t ora_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, const i
     }
     return k;
 }
+
+/* ---- prefix hash chain over token blocks [S] --------------------------------------
+ * The drawing's hash table ("cached_block_hash_to_block") keys every full block by a chain:
+ *     h0 = hash(seed, [t0 .. t(bs-1)]),  h_i = hash(h_(i-1), [tokens of block i])
+ * The pages do not name the hash.  Reading: FNV-1a 64 (offset basis 0xcbf29ce484222325,
+ * prime 0x100000001b3, each byte xored in, then multiplied) over the parent hash as 8
+ * little-endian bytes followed by the block's token ids as 4 little-endian bytes each.
+ * Only full blocks are hashed (a partial last block is not cacheable yet). */
+uint64_t ora_fnv1a64(const uint8_t *data, int64_t len)
+{
+    uint64_t h = 0xcbf29ce484222325ull;
+    for (int64_t i = 0; i < len; i++) {
+        h ^= data[i];
+        h *= 0x100000001b3ull;
+    }
+    return h;
+}
+
+/* tok_offsets [n_reqs + 1] is the CSR of each request's token ids in tokens.  Writes the
+ * hashes of every request's full blocks, in order, to out_hashes with CSR out_offsets
+ * [n_reqs + 1].  Returns the number of hashes, or -1 if the CSR is inconsistent or
+ * block_size <= 0. */
+int64_t ora_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const int32_t *tokens, int64_t n_tokens,
+                         int32_t block_size, uint64_t seed, int32_t *out_offsets, uint64_t *out_hashes)
+{
+    if (!csr_ok(tok_offsets, n_reqs, n_tokens) || block_size <= 0) return -1;
+    uint8_t *buf = (uint8_t *)malloc(8 + 4 * (size_t)block_size);
+    int64_t k = 0;
+    out_offsets[0] = 0;
+    for (int32_t r = 0; r < n_reqs; r++) {
+        int64_t n = tok_offsets[r + 1] - tok_offsets[r];
+        uint64_t parent = seed;
+        for (int64_t b = 0; b < n / block_size; b++) {
+            for (int j = 0; j < 8; j++) buf[j] = (uint8_t)(parent >> (8 * j));
+            for (int32_t t = 0; t < block_size; t++) {
+                uint32_t id = (uint32_t)tokens[tok_offsets[r] + b * block_size + t];
+                for (int j = 0; j < 4; j++) buf[8 + 4 * t + j] = (uint8_t)(id >> (8 * j));
+            }
+            parent = ora_fnv1a64(buf, 8 + 4 * (int64_t)block_size);
+            out_hashes[k++] = parent;
+        }
+        out_offsets[r + 1] = (int32_t)k;
+    }
+    free(buf);
+    return k;
+}

@@ -87,3 +87,14 @@ def read_clip_golden():
         a = [int(x) for x in left.split()]
         rows.append(dict(bs=a[0], window=a[1], n=a[2], ids=a[3:], want=[int(x) for x in right.split()]))
     return rows
+
+
+def read_fnv_golden():
+    rows = []
+    for line in open(golden_path("fnv1a64_vectors.txt"), encoding="utf-8"):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        data, want = [x.strip() for x in line.split(";")]
+        rows.append((b"" if data == "-" else bytes.fromhex(data), int(want, 16)))
+    return rows

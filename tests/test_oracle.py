@@ -301,9 +301,38 @@ def pin_clip_brute(lib):
         assert o[-1] == len(want)
 
 
+def pin_fnv_vectors(lib):
+    for data, want in H.read_fnv_golden():
+        assert oracle.fnv1a64(data, lib=lib) == want, data
+
+
+def pin_hash_chain(lib):
+    """Chain structure: h0 = hash(seed ‖ block 0), h_i = hash(h_(i-1) ‖ block i), full blocks only;
+    equal prefixes give equal hashes and a changed token changes its block's hash and every later one."""
+    rng = np.random.default_rng(7)
+    bs, seed = 4, 0x1234_5678_9ABC_DEF0
+    a = rng.integers(0, 128000, size=23).astype(np.int32)  # 5 full blocks and a partial one
+    b = a.copy()
+    b[13] += 1  # inside block 3
+    c = a[:9].copy()  # 2 full blocks and a partial
+    off, toks = W.csr([a, b, c])
+    o, h = oracle.block_hashes(off, toks, bs, seed, lib=lib)
+    assert o.tolist() == [0, 5, 10, 12]  # floor(23/4), floor(23/4), floor(9/4)
+    # explicit serialisation: parent as 8 little-endian bytes, then each token id as 4 little-endian bytes
+    h0 = oracle.fnv1a64(np.array([seed], "<u8").tobytes() + a[0:4].astype("<u4").tobytes(), lib=lib)
+    h1 = oracle.fnv1a64(np.array([h0], "<u8").tobytes() + a[4:8].astype("<u4").tobytes(), lib=lib)
+    assert int(h[0]) == h0 and int(h[1]) == h1
+    ha, hb, hc = h[0:5], h[5:10], h[10:12]
+    np.testing.assert_array_equal(ha[:3], hb[:3])  # shared prefix, shared hashes
+    assert all(int(x) != int(y) for x, y in zip(ha[3:], hb[3:]))  # the changed block and all after it
+    np.testing.assert_array_equal(hc, ha[:2])
+    _, h2 = oracle.block_hashes(off, toks, bs, seed + 1, lib=lib)
+    assert all(int(x) != int(y) for x, y in zip(h, h2))  # another seed changes every hash
+
+
 PINS = [pin_slot_golden, pin_slot_brute, pin_reshape_indexing, pin_pack_indexing, pin_pack_brute,
         pin_unpack_roundtrip, pin_unpack_other_ids, pin_unpack_remap_handworked, pin_unpack_brute,
-        pin_xfer_golden, pin_xfer_random, pin_clip_golden, pin_clip_brute]
+        pin_xfer_golden, pin_xfer_random, pin_clip_golden, pin_clip_brute, pin_fnv_vectors, pin_hash_chain]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -424,6 +453,10 @@ MUTANTS = [
     ("clip keeps one token too many", "? n - window : 0;", "? n - window - 1 : 0;"),
     ("clip drops the partial last block", "int64_t end = (n + block_size - 1) / block_size;", "int64_t end = n / block_size;"),
     ("clip ignores the window", "int64_t first = first_token / block_size;", "int64_t first = 0;"),
+    ("hash is FNV-1 (multiply before xor)", "h ^= data[i];\n        h *= 0x100000001b3ull;", "h *= 0x100000001b3ull;\n        h ^= data[i];"),
+    ("hash drops the parent", "buf[j] = (uint8_t)(parent >> (8 * j));", "buf[j] = 0;"),
+    ("hash big-endian token bytes", "buf[8 + 4 * t + j] = (uint8_t)(id >> (8 * j));", "buf[8 + 4 * t + j] = (uint8_t)(id >> (8 * (3 - j)));"),
+    ("hash covers the partial block", "for (int64_t b = 0; b < n / block_size; b++) {", "for (int64_t b = 0; b < (n + block_size - 1) / block_size; b++) {"),
 ]
 
 
