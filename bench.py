@@ -310,6 +310,7 @@ def run_ours(args):
 
     write_path = measure_write_path(step, dev) if step.n_tokens else None
     prior_art = measure_prior_art(step, dev, stream) if args.stage == "device" and not args.sw_window else None
+    prefix_hash = measure_prefix_hash(step, dev, stream) if case.req_tokens is not None else None
 
     host_link = None
     if args.stage == "host":
@@ -346,6 +347,8 @@ def run_ours(args):
         line["write_path"] = write_path
     if prior_art is not None:
         line["prior_art"] = prior_art
+    if prefix_hash is not None:
+        line["prefix_hash"] = prefix_hash
     if host_link is not None:
         line["host_link"] = host_link
         line["config"]["stage"] = "pinned host memory"
@@ -409,6 +412,32 @@ def measure_prior_art(step, dev, stream, reps: int = 5):
     if step.dst is not None:
         out["scatter_gbs"] = round(payload / (s_ms / reps * 1e-3) / 1e9, 1)
     return out
+
+
+def measure_prefix_hash(step, dev, stream, reps: int = 20) -> dict:
+    """kv_block_hashes over the batch's token ids (seeded synthetic ids, the case's request lengths)."""
+    import torch
+    from paged_kv_cache_81_gb300 import pagedkv as K
+
+    case = step.case
+    rng = np.random.default_rng(case.wl.seed + 7)
+    lens = case.req_tokens.astype(np.int64)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    toks = torch.from_numpy(rng.integers(0, 128000, size=int(off[-1])).astype(np.int32)).to(dev)
+    off_d = torch.from_numpy(off).to(dev)
+    bs = case.wl.src.block_size
+    o, h = K.kv_block_hashes(off_d, toks, bs, 81)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        K.kv_block_hashes(off_d, toks, bs, 81, o, h)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    us = a.elapsed_time(b) / reps * 1e3
+    n_hashes = int(sum(int(l) // bs for l in lens))
+    return {"requests": int(lens.shape[0]), "tokens": int(off[-1]), "hashes": n_hashes, "us": round(us, 2),
+            "hashes_per_s": round(n_hashes / (us * 1e-6), 1)}
 
 
 def measure_write_path(step, dev, iters: int = 200) -> dict:

@@ -241,6 +241,23 @@ KV_API int kv_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, const
                                int32_t *out_offsets, int32_t *out_ids, int64_t out_capacity, kv_stream_t stream);
 
 /*
+ * kv_block_hashes [S: the hash-table labels h0 = hash(seed, [t0..t1]), h1 = hash(h0, [t2..t3]), ...
+ * keying cached_block_hash_to_block]: the prefix hash chain over every request's FULL token
+ * blocks, h_i = H(h_(i-1), tokens of block i) with h_(-1) = seed, so requests sharing a prefix
+ * share its hashes.  The pages do not name H; this library reads it as FNV-1a 64 (basis
+ * 0xcbf29ce484222325, prime 0x100000001b3) over h_(i-1) as 8 little-endian bytes followed by the
+ * block's token ids as 4 little-endian bytes each.  A partial last block is not hashed.
+ * tok_offsets (n_reqs + 1) is the CSR of each request's token ids in tokens (device int32).
+ * Writes the hashes, in order, to out_hashes (device uint64, 8-byte aligned, out_capacity >=
+ * n_tokens / block_size) with CSR out_offsets (device int32, n_reqs + 1).  One thread walks
+ * each request's chain (FNV-1a is byte-serial), so the call is latency-bound; inconsistent
+ * offsets set KV_DERR_LIST and no write leaves out_hashes.  Limit: n_tokens < 2^31.
+ */
+KV_API int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const int32_t *tokens, int64_t n_tokens,
+                           int32_t block_size, uint64_t seed, int32_t *out_offsets, uint64_t *out_hashes,
+                           int64_t out_capacity, kv_stream_t stream);
+
+/*
  * kv_pack_blocks [N section 2.4 extract_kv_from_layer, F section 1.2]: for every
  * tensor t and run of `runs`, copies rows (t, src_block + m, p, o) - byte slice
  * [src_slice_off, src_slice_off + stage->slice_bytes) of each row - to the staging
