@@ -559,9 +559,15 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
         step.new_kv = views[0]
     secs = reduce_max(secs, dev)
     value = world * step.bytes().total * steps / secs / 1e9
-    return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": round(secs / steps * 1e3, 4),
-            "pipelined": "input copy of step k+1 overlaps step k"}
+    out = {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": steps, "ms_per_step": round(secs / steps * 1e3, 4),
+           "pipelined": "input copy of step k+1 overlaps step k"}
+    if host_rows is not None:
+        # this machine's host->device link, measured on the same pinned buffer: the bound of the leg
+        link = measure_host_link(host_rows.view(torch.uint8).reshape(-1), dev, comp, reps=3)["h2d_gbs"]
+        out["h2d_link_gbs"] = link
+        out["link_bound_ms_per_step"] = round(h2d / (link * 1e9) * 1e3, 4)
+    return out
 
 
 # ---------------------------------------------------------------------------
