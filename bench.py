@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the context measurements after the timed steps (write path, prior art, prefix hash)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     ap.add_argument("--stage", default="device", choices=["device", "host"],
                     help="staging buffer in HBM, or in pinned host memory (pack/unpack over the host link)")
@@ -308,9 +310,11 @@ def run_ours(args):
     if step.n_tokens:
         kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
 
-    write_path = measure_write_path(step, dev) if step.n_tokens else None
-    prior_art = measure_prior_art(step, dev, stream) if args.stage == "device" and not args.sw_window else None
-    prefix_hash = measure_prefix_hash(step, dev, stream) if case.req_tokens is not None else None
+    extras = not args.no_extras
+    write_path = measure_write_path(step, dev) if extras and step.n_tokens else None
+    prior_art = measure_prior_art(step, dev, stream) if extras and args.stage == "device" and not args.sw_window \
+        else None
+    prefix_hash = measure_prefix_hash(step, dev, stream) if extras and case.req_tokens is not None else None
 
     host_link = None
     if args.stage == "host":
@@ -485,67 +489,72 @@ def measure_host_link(host_buf, dev, stream, reps: int = 5) -> dict:
 def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
     """The same step through the public API from pinned host buffers.
 
-    Every step copies its inputs host->device (the new K/V rows of all layers, the token
-    and block lists) and reads its run count back device->host.  The 1.8 GB row copy of
-    step k+1 runs on a second stream while step k computes (two device buffers, ordered
-    by events); the lists are copied on the compute stream right before their step.  The
-    device error word is read once at the end (4 bytes)."""
+    Every step copies its inputs host->device (the new K/V rows of all layers and the token
+    and block lists) and reads its run count back device->host.  All input copies go on a
+    second stream into one of two buffer sets, so the copies of step k+1 run while step k
+    computes; events order each buffer set's reuse after the step that read it.  The device
+    error word is read once at the end (4 bytes)."""
     import torch
 
     comp = stream
     copy_stream = torch.cuda.Stream(dev)
-    bufs, views, host_rows = [], [], None
+    names = ["req_offsets", "src_ids", "dst_req_offsets", "dst_ids"]
+    if step.n_tokens:
+        names += ["block_table", "token_req", "token_pos"]
+    if step.sw_window:
+        names += ["req_tokens"]
+    host = {n: getattr(step, n).cpu().pin_memory() for n in names}
+    sets = [{n: getattr(step, n) for n in names}, {n: getattr(step, n).clone() for n in names}]
+    host_rows = None
     if step.n_tokens:
         big = step.new_kv[0]._base  # all tensors' new rows share one device buffer
-        bufs = [big, torch.empty_like(big)]
-        views = [[b[k] for k in range(b.shape[0])] for b in bufs]
+        rows = [big, torch.empty_like(big)]
+        for k in range(2):
+            sets[k]["_rows"] = rows[k]
+            sets[k]["_views"] = [rows[k][i] for i in range(rows[k].shape[0])]
         host_rows = torch.empty(big.shape, dtype=big.dtype, pin_memory=True)
         host_rows.copy_(big)
-    lists = [step.req_offsets, step.src_ids, step.dst_req_offsets, step.dst_ids]
-    if step.n_tokens:
-        lists += [step.block_table, step.token_req, step.token_pos]
-    small = [(t, t.cpu().pin_memory()) for t in lists]
     steps = max(1, min(args.steps, 100))
     n_runs_host = torch.empty(steps, dtype=torch.int32, pin_memory=True)
     copied = [torch.cuda.Event() for _ in range(2)]
     freed = [torch.cuda.Event() for _ in range(2)]
-    h2d = sum(h.numel() * h.element_size() for _, h in small) + (host_rows.numel() * 2 if host_rows is not None else 0)
+    h2d = sum(h.numel() * h.element_size() for h in host.values()) + (
+        host_rows.numel() * host_rows.element_size() if host_rows is not None else 0)
     d2h = 4
 
     def issue_copy(k):
-        if host_rows is None:
-            return
         b = k % 2
         if k >= 2:
-            copy_stream.wait_event(freed[b])  # step k-2 has finished reading this buffer
+            copy_stream.wait_event(freed[b])  # step k-2 is done with this buffer set
         with torch.cuda.stream(copy_stream):
-            bufs[b].copy_(host_rows, non_blocking=True)
+            for n in names:
+                sets[b][n].copy_(host[n], non_blocking=True)
+            if host_rows is not None:
+                sets[b]["_rows"].copy_(host_rows, non_blocking=True)
         copied[b].record(copy_stream)
 
     def run_step(k):
-        for d, h in small:
-            d.copy_(h, non_blocking=True)
+        b = k % 2
+        comp.wait_event(copied[b])
+        for n in names:
+            setattr(step, n, sets[b][n])
         if host_rows is not None:
-            b = k % 2
-            comp.wait_event(copied[b])
-            step.new_kv = views[b]
-        step.write_tokens()
-        if host_rows is not None:
-            freed[k % 2].record(comp)
-        step.build()
-        step.pack()
-        step.unpack()
+            step.new_kv = sets[b]["_views"]
+        step.run()
+        freed[b].record(comp)
         n_runs_host[k:k + 1].copy_(step.xfer.n_runs, non_blocking=True)
 
     def run(n):
         issue_copy(0)
-        issue_copy(1)
+        if n > 1:
+            issue_copy(1)
         for k in range(n):
             run_step(k)
-            issue_copy(k + 2) if k + 2 < n else None
-        torch.cuda.synchronize(dev)
+            if k + 2 < n:
+                issue_copy(k + 2)
 
     run(min(3, steps))
+    torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -555,13 +564,15 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
     secs = time.perf_counter() - t0
     if err:
         raise RuntimeError(f"device error word {err:#x} in the end-to-end run")
+    for n in names:  # leave the step on its original buffers
+        setattr(step, n, sets[0][n])
     if host_rows is not None:
-        step.new_kv = views[0]
+        step.new_kv = sets[0]["_views"]
     secs = reduce_max(secs, dev)
     value = world * step.bytes().total * steps / secs / 1e9
     out = {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": steps, "ms_per_step": round(secs / steps * 1e3, 4),
-           "pipelined": "input copy of step k+1 overlaps step k"}
+           "pipelined": "input copies of step k+1 (second stream, double-buffered) overlap step k"}
     if host_rows is not None:
         # this machine's host->device link, measured on the same pinned buffer: the bound of the leg
         link = measure_host_link(host_rows.view(torch.uint8).reshape(-1), dev, comp, reps=3)["h2d_gbs"]
