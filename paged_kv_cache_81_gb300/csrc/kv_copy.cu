@@ -39,13 +39,17 @@ using pkv::REMAP;
 #ifndef PKV_COPY_MIN_CTAS
 #define PKV_COPY_MIN_CTAS 1  // launch-bounds hint: resident CTAs per SM the register budget must allow
 #endif
+#ifndef PKV_ROWS_MIN_CTAS
+#define PKV_ROWS_MIN_CTAS 1  // the same hint for the ROWS and REMAP modes (more index arithmetic per chunk)
+#endif
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = PKV_COPY_UNROLL;
 constexpr uint32_t kPieceChunks = 1024;  // 16 KiB
 
 template <int MODE, bool PACK>
-__global__ void __launch_bounds__(kThreads, PKV_COPY_MIN_CTAS) copy_runs_kernel(const __grid_constant__ CopyParams p)
+__global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTAS : PKV_COPY_MIN_CTAS)
+    copy_runs_kernel(const __grid_constant__ CopyParams p)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
