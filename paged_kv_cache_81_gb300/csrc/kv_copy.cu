@@ -7,10 +7,10 @@
 // 机制", section 4.2 (_build_transfer_params).
 //
 // Work decomposition: an item is one piece (at most kPieceChunks 16-byte chunks) of one
-// (tensor, run).  Items are numbered tensor-major, so consecutive warps write adjacent
-// staging ranges; the grid is persistent (resident CTAs on every SM) and walks the items
-// with a warp stride.  Inside a piece each lane keeps kUnroll 16-byte loads in flight
-// before storing them.
+// (tensor, run).  Items are numbered piece-major, then tensor, then run, so consecutive warps
+// write adjacent staging ranges and no warp keeps drawing empty pieces; the grid is
+// persistent (resident CTAs on every SM) and walks the items with a warp stride.  Inside a
+// piece each lane keeps kUnroll 16-byte loads in flight before storing them.
 //
 // Address modes of the cache side (the staging side is always linear):
 //   MERGED  a run is one contiguous span (dense blocks, block_stride == staged block bytes)
@@ -100,9 +100,13 @@ __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTA
                 continue;
             }
             const int32_t s0 = p.src_req_offsets[r];
-            j0 = (int32_t)((run.stage_block - s0) * (int64_t)p.div_bs.d);
             const int32_t d0 = p.dst_req_offsets[r];
             dn = p.dst_req_offsets[r + 1] - d0;
+            if (run.stage_block < s0 || dn < 0 || d0 < 0) {  // offsets that do not match the runs
+                if (first_piece && lane == 0) pkv::set_error(p.err, KV_DERR_DST_TABLE);
+                continue;
+            }
+            j0 = (int32_t)((run.stage_block - s0) * (int64_t)p.div_bs.d);
             dl = p.dst_ids + d0;
         } else {
             blk = PACK ? run.src_block : run.dst_block;
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTA
                     } else {  // REMAP: staged token j of the request -> destination slot
                         const uint32_t j = (uint32_t)j0 + m * p.div_bs.d + o;
                         const uint32_t dq = pkv::fdiv(j, p.div_dbs);
-                        if ((int32_t)dq >= dn) {
+                        if (dq >= (uint32_t)dn) {
                             pkv::set_error(p.err, KV_DERR_DST_TABLE);
                             continue;
                         }

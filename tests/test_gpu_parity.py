@@ -325,3 +325,31 @@ def test_more_tensors_than_one_launch_carries(layout):
             np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
         for a, b in zip(d_dev, dh):
             np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+
+
+def test_remap_with_offsets_that_do_not_match_the_runs():
+    """Unpack remap given source offsets that disagree with the runs (a request said to start past
+    its runs): those runs are skipped and flagged, nothing is read or written out of place."""
+    sg = W.CacheGeom("separate", 16, 4, 1, 64)  # 128-byte rows
+    dg = W.CacheGeom("separate", 64, 1, 1, 64)  # destination block size 1
+    rng = np.random.default_rng(12)
+    src = W.host_cache_tensors(sg, 1, rng)
+    dst = W.host_cache_tensors(dg, 1, rng)
+    off, ids = W.csr([[3, 4], [9]])
+    doff, dids = W.csr([list(range(0, 8)), list(range(8, 12))])  # 8 and 4 one-slot blocks
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    d_dev = W.to_device_bf16(dst, "cuda")
+    scache = K.PagedCache.from_tensors(W.to_device_bf16(src, "cuda"), "separate")
+    dcache = K.PagedCache.from_tensors(d_dev, "separate")
+    x = K.kv_build_xfer_list(t(off), t(ids), None, 2)
+    stage = K.kv_pack_blocks(scache, x, 3)
+    bad_off = t([0, 3, 3])  # request 1 "starts" at entry 3, after its run at entry 2
+    K.kv_unpack_blocks(dcache, stage, x, 3, 4, None, 0, bad_off, t(doff), t(dids))
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() & K.KV_DERR_DST_TABLE
+    # request 0's run still lands in slots 0..7; the rest of the destination is untouched
+    got = d_dev[0].cpu().view(torch.int16).numpy().view(np.uint16).reshape(64, -1)
+    want = dst[0].reshape(64, -1).copy()
+    st = stage.cpu().numpy().reshape(3 * 4, -1).view(np.uint16)
+    want[0:8] = st[0:8]
+    np.testing.assert_array_equal(got, want)
