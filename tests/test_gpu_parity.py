@@ -353,3 +353,24 @@ def test_remap_with_offsets_that_do_not_match_the_runs():
     st = stage.cpu().numpy().reshape(3 * 4, -1).view(np.uint16)
     want[0:8] = st[0:8]
     np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("wl", [W.small(W.PAGE), W.small(W.MID), W.small(W.ASYM)], ids=lambda w: w.name)
+def test_staging_guard_canaries(wl):
+    """Canary bytes before and after the staging region survive pack (both copy engines' paths)."""
+    case = W.make_case(wl)
+    src, dst, new = G.host_inputs(wl, case, seed=99)
+    scache = K.PagedCache.from_tensors(W.to_device_bf16(src, "cuda"), wl.src.layout)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    cap = K.default_max_run_blocks(wl.src.n_planes * wl.src.block_size * wl.moved_slice)
+    x = K.kv_build_xfer_list(t(case.req_offsets), t(case.src_ids), None, cap)
+    n = G._stage_len(wl, case)
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    K.kv_pack_blocks(scache, x, case.n_blocks, buf[guard:guard + n], wl.slice_off, wl.moved_slice)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() == 0
+    b = buf.cpu().numpy()
+    assert (b[:guard] == 0xA5).all() and (b[guard + n:] == 0xA5).all()
+    want = oracle.pack(H.ora_cache(wl.src, src), case.req_offsets, case.src_ids, wl.slice_off, wl.moved_slice)
+    np.testing.assert_array_equal(b[guard:guard + n], want)
