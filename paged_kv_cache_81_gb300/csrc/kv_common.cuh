@@ -46,20 +46,36 @@ __host__ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f)
 // 16-byte global accesses.  Cache rows are read once (no L1 allocation); staging
 // and cache writes are streaming (evict-first) stores.
 // ---------------------------------------------------------------------------
+#ifndef PKV_LD_NO_ALLOCATE
+#define PKV_LD_NO_ALLOCATE 1  // 0: read-only loads that may allocate in L1
+#endif
+#ifndef PKV_ST_STREAMING
+#define PKV_ST_STREAMING 1  // 0: plain write-back stores
+#endif
+
 __device__ __forceinline__ uint4 ld_once(const void *p)
 {
     uint4 v;
+#if PKV_LD_NO_ALLOCATE
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+#else
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+#endif
     return v;
 }
 
 __device__ __forceinline__ void st_stream(void *p, const uint4 &v)
 {
+#if PKV_ST_STREAMING
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+#else
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+#endif
 }
 
 __device__ __forceinline__ void set_error(int *err, int bits)

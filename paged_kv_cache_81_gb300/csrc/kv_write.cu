@@ -50,6 +50,7 @@ struct ReshapeParams {
     FastDiv div_cpr;     // chunks per row
     FastDiv div_planes;
     FastDiv div_bs;
+    FastDiv div_tokens;
     int32_t n_planes;
     int *err;
     uint64_t dst[pkv::kMaxTensorsPerLaunch];
@@ -58,6 +59,9 @@ struct ReshapeParams {
 
 #ifndef PKV_RESHAPE_UNROLL
 #define PKV_RESHAPE_UNROLL 4  // 16-byte loads each thread keeps in flight
+#endif
+#ifndef PKV_RESHAPE_PLANE_MAJOR
+#define PKV_RESHAPE_PLANE_MAJOR 0  // 1: order work (plane, token, chunk) instead of (token, plane, chunk)
 #endif
 constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
 
@@ -77,8 +81,14 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_con
             if (idx >= p.total) continue;
             const uint32_t row = pkv::fdiv((uint32_t)idx, p.div_cpr);
             const uint32_t chunk = (uint32_t)idx - row * p.div_cpr.d;
+#if PKV_RESHAPE_PLANE_MAJOR
+            // rows ordered (plane, token): neighbouring threads take neighbouring tokens of one plane
+            const uint32_t plane = pkv::fdiv(row, p.div_tokens);
+            const uint32_t tok = row - plane * p.div_tokens.d;
+#else
             const uint32_t tok = pkv::fdiv(row, p.div_planes);
             const uint32_t plane = row - tok * p.div_planes.d;
+#endif
             const int64_t s = p.slot[tok];
             if (s < 0) continue;  // padding token
             if (s >= (int64_t)p.slot_limit) {
@@ -156,6 +166,7 @@ int kv_reshape_and_cache(const kv_cache_desc *cache, const uint64_t *new_kv, int
     p.div_cpr = pkv::make_fastdiv((uint32_t)cpr);
     p.div_planes = pkv::make_fastdiv((uint32_t)cache->n_planes);
     p.div_bs = pkv::make_fastdiv((uint32_t)cache->block_size);
+    p.div_tokens = pkv::make_fastdiv((uint32_t)n_tokens);
     p.n_planes = cache->n_planes;
     p.err = dev->err_word;
 
