@@ -17,6 +17,7 @@ host cores on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 from paged_kv_cache_81_gb300 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
+PG_TIMEOUT_S = 300  # process-group timeout under torchrun
 KERNEL_NAMES = ("slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack")
 COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_copy.cuh",
                 "paged_kv_cache_81_gb300/csrc/kv_bulk.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
@@ -213,7 +215,8 @@ def run_ours(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
-        dist.init_process_group("nccl")
+        # a rank that dies makes the others' next collective fail within this bound instead of hanging
+        dist.init_process_group("nccl", timeout=datetime.timedelta(seconds=PG_TIMEOUT_S))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 

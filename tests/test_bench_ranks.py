@@ -82,3 +82,45 @@ def test_reference_arm_prints_one_line():
 def test_reference_arm_other_ranks_print_nothing():
     r = _reference({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def _rank_fails(rank, world, port, q):
+    import datetime
+    import torch
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
+    import bench
+
+    if rank == 1:
+        os._exit(3)  # this rank dies between steps, before the timing reduction
+    import time
+    t0 = time.time()
+    try:
+        bench.reduce_max(1.0, torch.device("cpu"))
+        outcome = "returned"
+    except Exception as e:  # the survivor learns of the failure instead of waiting forever
+        outcome = type(e).__name__
+    q.put((rank, outcome, time.time() - t0))
+    q.close()
+    q.join_thread()  # flush the message before leaving without tearing down the broken group
+    os._exit(0)
+
+
+def test_a_dead_rank_fails_the_reduction_instead_of_hanging():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_fails, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+    assert procs[1].exitcode == 3
+    rank, outcome, secs = q.get(timeout=10)
+    assert rank == 0 and outcome != "returned" and secs < 60, (outcome, secs)
