@@ -189,11 +189,16 @@ class PagedCache:
         return cls(tensors, int(nb), int(bs), planes, int(row), int(block), int(plane), int(token))
 
     def desc(self) -> KvCacheDesc:
-        n = len(self.tensors)
-        self._bases = (ctypes.c_uint64 * max(1, n))(*[x.data_ptr() for x in self.tensors])
-        return KvCacheDesc(n, self.block_size, self.n_planes, self.row_bytes, self.num_blocks, self.block_stride,
-                           self.plane_stride, self.token_stride,
-                           ctypes.cast(self._bases, ctypes.POINTER(ctypes.c_uint64)))
+        """The kv_cache_desc of these tensors, built once and rebuilt only if a tensor moved."""
+        ptrs = tuple(x.data_ptr() for x in self.tensors)
+        if getattr(self, "_desc_ptrs", None) != ptrs:
+            n = len(ptrs)
+            self._bases = (ctypes.c_uint64 * max(1, n))(*ptrs)
+            self._desc = KvCacheDesc(n, self.block_size, self.n_planes, self.row_bytes, self.num_blocks,
+                                     self.block_stride, self.plane_stride, self.token_stride,
+                                     ctypes.cast(self._bases, ctypes.POINTER(ctypes.c_uint64)))
+            self._desc_ptrs = ptrs
+        return self._desc
 
 
 def stage_desc(n_blocks: int, n_tensors: int, n_planes: int, block_size: int, slice_bytes: int) -> KvStageDesc:
@@ -247,6 +252,15 @@ class XferList:
         self.max_run_blocks = int(max_run_blocks)
         self.runs = torch.empty((max(1, self.capacity), RUN_WORDS), dtype=torch.int32, device=device)
         self.n_runs = torch.zeros(1, dtype=torch.int32, device=device)
+        self._ws = None
+        self._ws_blocks = -1
+
+    def workspace(self, n_blocks: int) -> torch.Tensor:
+        """A builder workspace for lists of n_blocks entries, kept with this list for reuse."""
+        if self._ws is None or self._ws_blocks < n_blocks:
+            self._ws = torch.empty(kv_xfer_workspace_bytes(n_blocks), dtype=torch.uint8, device=self.runs.device)
+            self._ws_blocks = n_blocks
+        return self._ws
 
     def host(self) -> dict:
         """Copy the runs to the host as numpy columns (synchronises)."""
@@ -266,9 +280,8 @@ def kv_build_xfer_list(req_offsets: torch.Tensor, src_ids: torch.Tensor, dst_ids
     n = src_ids.shape[0]
     if out is None:
         out = XferList(n, src_ids.device, max_run_blocks)
-    ws_bytes = kv_xfer_workspace_bytes(n)
     if workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=src_ids.device)
+        workspace = out.workspace(n)
     _check("kv_build_xfer_list", load().kv_build_xfer_list(
         _ptr(req_offsets), req_offsets.shape[0] - 1, _ptr(src_ids), _ptr(dst_ids), n, int(max_run_blocks),
         _ptr(out.runs), out.capacity, _ptr(out.n_runs), _ptr(workspace), workspace.numel(), _stream(stream)))
