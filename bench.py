@@ -318,6 +318,7 @@ def run_ours(args):
     prior_art = measure_prior_art(step, dev, stream) if extras and args.stage == "device" and not args.sw_window \
         else None
     prefix_hash = measure_prefix_hash(step, dev, stream) if extras and case.req_tokens is not None else None
+    single = measure_single_request(step, dev) if extras and args.stage == "device" and not args.sw_window else None
 
     host_link = None
     if args.stage == "host":
@@ -356,6 +357,8 @@ def run_ours(args):
         line["prior_art"] = prior_art
     if prefix_hash is not None:
         line["prefix_hash"] = prefix_hash
+    if single is not None:
+        line["single_request"] = single
     if host_link is not None:
         line["host_link"] = host_link
         line["config"]["stage"] = "pinned host memory"
@@ -445,6 +448,46 @@ def measure_prefix_hash(step, dev, stream, reps: int = 20) -> dict:
     n_hashes = int(sum(int(l) // bs for l in lens))
     return {"requests": int(lens.shape[0]), "tokens": int(off[-1]), "hashes": n_hashes, "us": round(us, 2),
             "hashes_per_s": round(n_hashes / (us * 1e-6), 1)}
+
+
+def measure_single_request(step, dev, blocks: int = 64, iters: int = 200):
+    """Latency of moving one request: build + pack + unpack of its first `blocks` blocks in every
+    tensor of the same caches (wall clock per transfer, issued call by call and from a CUDA graph)."""
+    import torch
+    from paged_kv_cache_81_gb300.step import TransferStep
+
+    wl, case = step.wl, step.case
+    n = min(blocks, int(case.req_offsets[1] - case.req_offsets[0]))
+    if n <= 0 or step.dst is None:
+        return None
+    one = W.Case(wl, np.array([0, n], np.int32), case.src_ids[:n].copy(), np.array([0, n], np.int32),
+                 case.dst_ids[:n].copy() if step.equal else case.dst_ids[:case.dst_req_offsets[1]].copy(),
+                 req_tokens=None)
+    if not step.equal:  # the receiver's list of the first request, as many blocks as the staged tokens need
+        one.dst_req_offsets = np.array([0, one.dst_ids.shape[0]], np.int32)
+    small = TransferStep(wl, one, step.src.tensors, step.dst.tensors, device=dev)
+
+    def transfer():
+        small.build()
+        small.pack()
+        small.unpack()
+
+    def wall(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(iters):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / iters * 1e6
+
+    eager = wall(transfer)
+    graph = small.capture(transfer)
+    replay = wall(graph.replay)
+    del graph
+    return {"blocks": n, "tensors": len(step.src.tensors), "bytes_moved": small.bytes().pack + small.bytes().unpack,
+            "eager_us": round(eager, 2), "graph_us": round(replay, 2)}
 
 
 def measure_write_path(step, dev, iters: int = 200) -> dict:
