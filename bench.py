@@ -492,7 +492,8 @@ def measure_single_request(step, dev, blocks: int = 64, iters: int = 200):
 
 def measure_write_path(step, dev, iters: int = 200) -> dict:
     """Wall-clock cost of the new-token write (kv_slot_mapping + kv_reshape_and_cache) issued
-    call by call from Python, and replayed from a CUDA graph of the same two calls."""
+    call by call from Python and replayed from a CUDA graph; the same for kv_write_tokens, the
+    two calls fused into one launch."""
     import torch
 
     def timed(fn):
@@ -509,8 +510,13 @@ def measure_write_path(step, dev, iters: int = 200) -> dict:
     graph = step.capture(step.write_tokens)
     replay = timed(graph.replay)
     del graph
+    fused_eager = timed(step.write_tokens_fused)
+    graph = step.capture(step.write_tokens_fused)
+    fused_replay = timed(graph.replay)
+    del graph
     return {"tokens": step.n_tokens, "tensors": len(step.src.tensors), "eager_us_per_step": round(eager, 2),
-            "graph_us_per_step": round(replay, 2)}
+            "graph_us_per_step": round(replay, 2), "fused_eager_us_per_step": round(fused_eager, 2),
+            "fused_graph_us_per_step": round(fused_replay, 2)}
 
 
 def measure_host_link(host_buf, dev, stream, reps: int = 5) -> dict:

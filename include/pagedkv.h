@@ -169,6 +169,20 @@ KV_API int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t m
 KV_API int kv_reshape_and_cache(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride,
                          const int64_t *slot, int64_t n_tokens, kv_stream_t stream);
 
+/*
+ * kv_write_tokens [S "batch tensor 组装", "Paged kv cache"]: kv_slot_mapping and
+ * kv_reshape_and_cache in one launch per 128 tensors.  Each token's slot is looked up in the
+ * block table inside the row-copy kernel (block_size = cache->block_size), so a decode step's
+ * cache write is a single kernel.  Arguments as for the two calls; slot_out (device int64
+ * [n_tokens], may be NULL) receives the slots, -1 for invalid tokens, exactly as
+ * kv_slot_mapping writes them.  An invalid token sets KV_DERR_TABLE and writes nothing; a slot
+ * beyond the cache sets KV_DERR_SLOT.  Limits as for kv_reshape_and_cache.
+ */
+KV_API int kv_write_tokens(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride,
+                           const int32_t *block_table, int32_t n_reqs, int32_t max_blocks_per_req,
+                           int64_t bt_row_stride, const int32_t *token_req, const int32_t *token_pos,
+                           int64_t n_tokens, int64_t *slot_out, kv_stream_t stream);
+
 /* Device workspace bytes kv_build_xfer_list needs for a list of n_blocks entries. */
 KV_API int kv_xfer_workspace_bytes(int64_t n_blocks, int64_t *bytes_out);
 

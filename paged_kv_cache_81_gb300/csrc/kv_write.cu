@@ -40,7 +40,15 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(const int32_t *__rest
 // threads cover consecutive chunks of one row, so every row is read and written as
 // whole coalesced segments.
 struct ReshapeParams {
-    const int64_t *slot;
+    const int64_t *slot;  // slots of the tokens (reshape_and_cache), or null when FUSED
+    // FUSED (kv_write_tokens): each token's slot is looked up in the block table here
+    const int32_t *table;
+    const int32_t *token_req;
+    const int32_t *token_pos;
+    int64_t *slot_out;  // optional: the looked-up slots are also written here (first launch only)
+    int64_t table_row_stride;
+    int32_t n_reqs;
+    int32_t max_blocks;
     int64_t src_token_stride;
     int64_t block_stride;
     int64_t plane_stride;
@@ -60,12 +68,34 @@ struct ReshapeParams {
 #ifndef PKV_RESHAPE_UNROLL
 #define PKV_RESHAPE_UNROLL 4  // 16-byte loads each thread keeps in flight
 #endif
+#ifndef PKV_RESHAPE_MIN_CTAS
+#define PKV_RESHAPE_MIN_CTAS 6  // launch-bounds hint: resident CTAs per SM the register budget must allow
+#endif
+#ifndef PKV_RESHAPE_LOADS_FIRST
+#define PKV_RESHAPE_LOADS_FIRST 1  // 0: resolve each row's slot before issuing its load
+#endif
 #ifndef PKV_RESHAPE_PLANE_MAJOR
 #define PKV_RESHAPE_PLANE_MAJOR 0  // 1: order work (plane, token, chunk) instead of (token, plane, chunk)
 #endif
 constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
 
-__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p)
+// The slot of token `tok`: the block table's entry for the token's logical block times the
+// block size plus the offset in the block, or -1 for an invalid token.
+__device__ __forceinline__ int64_t table_slot(const ReshapeParams &p, uint32_t tok)
+{
+    const int32_t req = p.token_req[tok];
+    const int32_t pos = p.token_pos[tok];
+    if (req < 0 || req >= p.n_reqs || pos < 0) return -1;
+    const uint32_t q = pkv::fdiv((uint32_t)pos, p.div_bs);
+    if (q >= (uint32_t)p.max_blocks) return -1;
+    const int32_t block = p.table[(int64_t)req * p.table_row_stride + q];
+    if (block < 0) return -1;
+    return (int64_t)block * p.div_bs.d + ((uint32_t)pos - q * p.div_bs.d);
+}
+
+template <bool FUSED>
+__global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
+    reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p)
 {
     const int t = blockIdx.y;
     uint8_t *const dst = reinterpret_cast<uint8_t *>(p.dst[t]);
@@ -73,39 +103,117 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const __grid_con
     for (uint64_t base = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; base < p.total;
          base += stride * kReshapeUnroll) {
         uint4 v[kReshapeUnroll];
-        uint8_t *d[kReshapeUnroll];
+        uint32_t tok[kReshapeUnroll], plane[kReshapeUnroll], chunk[kReshapeUnroll];
+        // The row loads do not depend on the slot (only the store address does): issue them
+        // all first, then resolve the slots while they are in flight.
 #pragma unroll
         for (int u = 0; u < kReshapeUnroll; u++) {
-            d[u] = nullptr;
             const uint64_t idx = base + (uint64_t)u * stride;
+            tok[u] = 0xffffffffu;
             if (idx >= p.total) continue;
             const uint32_t row = pkv::fdiv((uint32_t)idx, p.div_cpr);
-            const uint32_t chunk = (uint32_t)idx - row * p.div_cpr.d;
+            chunk[u] = (uint32_t)idx - row * p.div_cpr.d;
 #if PKV_RESHAPE_PLANE_MAJOR
             // rows ordered (plane, token): neighbouring threads take neighbouring tokens of one plane
-            const uint32_t plane = pkv::fdiv(row, p.div_tokens);
-            const uint32_t tok = row - plane * p.div_tokens.d;
+            plane[u] = pkv::fdiv(row, p.div_tokens);
+            tok[u] = row - plane[u] * p.div_tokens.d;
 #else
-            const uint32_t tok = pkv::fdiv(row, p.div_planes);
-            const uint32_t plane = row - tok * p.div_planes.d;
+            tok[u] = pkv::fdiv(row, p.div_planes);
+            plane[u] = row - tok[u] * p.div_planes.d;
 #endif
-            const int64_t s = p.slot[tok];
-            if (s < 0) continue;  // padding token
+#if PKV_RESHAPE_LOADS_FIRST
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane[u]]);
+            v[u] = pkv::ld_once(src + (int64_t)tok[u] * p.src_token_stride + (int64_t)chunk[u] * 16);
+#endif
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            if (tok[u] == 0xffffffffu) continue;
+            int64_t s;
+            if (FUSED) {
+                s = table_slot(p, tok[u]);
+                const bool first = t == 0 && plane[u] == 0 && chunk[u] == 0;  // one thread per token reports
+                if (first && p.slot_out != nullptr) p.slot_out[tok[u]] = s;
+                if (s < 0) {
+                    if (first) pkv::set_error(p.err, KV_DERR_TABLE);
+                    continue;
+                }
+            } else {
+                s = p.slot[tok[u]];
+                if (s < 0) continue;  // padding token
+            }
             if (s >= (int64_t)p.slot_limit) {
                 pkv::set_error(p.err, KV_DERR_SLOT);
                 continue;
             }
+#if !PKV_RESHAPE_LOADS_FIRST
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane[u]]);
+            v[u] = pkv::ld_once(src + (int64_t)tok[u] * p.src_token_stride + (int64_t)chunk[u] * 16);
+#endif
             const uint32_t block = pkv::fdiv((uint32_t)s, p.div_bs);
             const uint32_t off = (uint32_t)s - block * p.div_bs.d;
-            d[u] = dst + (int64_t)block * p.block_stride + (int64_t)plane * p.plane_stride +
-                   (int64_t)off * p.token_stride + (int64_t)chunk * 16;
-            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane]);
-            v[u] = pkv::ld_once(src + (int64_t)tok * p.src_token_stride + (int64_t)chunk * 16);
+            pkv::st_stream(dst + (int64_t)block * p.block_stride + (int64_t)plane[u] * p.plane_stride +
+                               (int64_t)off * p.token_stride + (int64_t)chunk[u] * 16,
+                           v[u]);
         }
-#pragma unroll
-        for (int u = 0; u < kReshapeUnroll; u++)
-            if (d[u] != nullptr) pkv::st_stream(d[u], v[u]);
     }
+}
+
+// Validation and launches shared by kv_reshape_and_cache and kv_write_tokens.
+template <bool FUSED>
+int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride, int64_t n_tokens,
+                ReshapeParams p, cudaStream_t stream)
+{
+    int st = pkv::check_cache(cache);
+    if (st != KV_OK) return st;
+    if (n_tokens < 0 || new_token_stride < 0) return KV_ERR_INVALID_ARG;
+    if (n_tokens == 0 || cache->n_tensors == 0) return KV_OK;
+    if (new_kv == nullptr) return KV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(new_token_stride)) return KV_ERR_ALIGN;
+    if (new_token_stride < cache->row_bytes) return KV_ERR_RANGE;
+    for (int64_t k = 0; k < (int64_t)cache->n_tensors * cache->n_planes; k++) {
+        if (new_kv[k] == 0) return KV_ERR_INVALID_ARG;
+        if (new_kv[k] & 15u) return KV_ERR_ALIGN;
+    }
+    const int64_t slot_limit = cache->num_blocks * (int64_t)cache->block_size;
+    const int64_t cpr = cache->row_bytes / 16;
+    const int64_t total = n_tokens * cache->n_planes * cpr;
+    if (slot_limit >= (1ll << 31) || total >= (1ll << 31) || cpr >= (1ll << 31)) return KV_ERR_UNSUPPORTED;
+    const pkv::DeviceInfo *dev = pkv::current_device();
+    if (dev == nullptr) return KV_ERR_CUDA;
+
+    p.src_token_stride = new_token_stride;
+    p.block_stride = cache->block_stride;
+    p.plane_stride = cache->plane_stride;
+    p.token_stride = cache->token_stride;
+    p.total = (uint32_t)total;
+    p.slot_limit = (uint32_t)slot_limit;
+    p.div_cpr = pkv::make_fastdiv((uint32_t)cpr);
+    p.div_planes = pkv::make_fastdiv((uint32_t)cache->n_planes);
+    p.div_bs = pkv::make_fastdiv((uint32_t)cache->block_size);
+    p.div_tokens = pkv::make_fastdiv((uint32_t)n_tokens);
+    p.n_planes = cache->n_planes;
+    p.err = dev->err_word;
+
+    const int threads = 256;
+    const int64_t per_tensor_ctas = (total + (int64_t)threads * kReshapeUnroll - 1) / ((int64_t)threads * kReshapeUnroll);
+    int64_t *slot_out = p.slot_out;
+    for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
+        const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
+        for (int32_t t = 0; t < nt; t++) {
+            p.dst[t] = cache->base[t0 + t];
+            for (int32_t pl = 0; pl < cache->n_planes; pl++)
+                p.src[t * cache->n_planes + pl] = new_kv[(int64_t)(t0 + t) * cache->n_planes + pl];
+        }
+        p.slot_out = t0 == 0 ? slot_out : nullptr;
+        // about four waves of 8 resident CTAs per SM over all tensors of the launch
+        const int64_t cap = std::max<int64_t>(1, ((int64_t)dev->num_sms * 8 * 4 + nt - 1) / nt);
+        const dim3 grid((unsigned)std::min(per_tensor_ctas, cap), (unsigned)nt);
+        reshape_and_cache_kernel<FUSED><<<grid, threads, 0, stream>>>(p);
+        st = pkv::cuda_status(cudaGetLastError());
+        if (st != KV_OK) return st;
+    }
+    return KV_OK;
 }
 
 }  // namespace
@@ -137,56 +245,31 @@ int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t max_bloc
 int kv_reshape_and_cache(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride,
                          const int64_t *slot, int64_t n_tokens, kv_stream_t stream)
 {
-    int st = pkv::check_cache(cache);
-    if (st != KV_OK) return st;
-    if (n_tokens < 0 || new_token_stride < 0) return KV_ERR_INVALID_ARG;
-    if (n_tokens == 0 || cache->n_tensors == 0) return KV_OK;
-    if (slot == nullptr || new_kv == nullptr) return KV_ERR_INVALID_ARG;
-    if (!pkv::aligned16(new_token_stride)) return KV_ERR_ALIGN;
-    if (new_token_stride < cache->row_bytes) return KV_ERR_RANGE;
-    for (int64_t k = 0; k < (int64_t)cache->n_tensors * cache->n_planes; k++) {
-        if (new_kv[k] == 0) return KV_ERR_INVALID_ARG;
-        if (new_kv[k] & 15u) return KV_ERR_ALIGN;
-    }
-    const int64_t slot_limit = cache->num_blocks * (int64_t)cache->block_size;
-    const int64_t cpr = cache->row_bytes / 16;
-    const int64_t total = n_tokens * cache->n_planes * cpr;
-    if (slot_limit >= (1ll << 31) || total >= (1ll << 31) || cpr >= (1ll << 31)) return KV_ERR_UNSUPPORTED;
-    const pkv::DeviceInfo *dev = pkv::current_device();
-    if (dev == nullptr) return KV_ERR_CUDA;
-
+    if (n_tokens > 0 && slot == nullptr) return KV_ERR_INVALID_ARG;
     ReshapeParams p{};
     p.slot = slot;
-    p.src_token_stride = new_token_stride;
-    p.block_stride = cache->block_stride;
-    p.plane_stride = cache->plane_stride;
-    p.token_stride = cache->token_stride;
-    p.total = (uint32_t)total;
-    p.slot_limit = (uint32_t)slot_limit;
-    p.div_cpr = pkv::make_fastdiv((uint32_t)cpr);
-    p.div_planes = pkv::make_fastdiv((uint32_t)cache->n_planes);
-    p.div_bs = pkv::make_fastdiv((uint32_t)cache->block_size);
-    p.div_tokens = pkv::make_fastdiv((uint32_t)n_tokens);
-    p.n_planes = cache->n_planes;
-    p.err = dev->err_word;
+    return launch_rows<false>(cache, new_kv, new_token_stride, n_tokens, p, (cudaStream_t)stream);
+}
 
-    const int threads = 256;
-    const int64_t per_tensor_ctas = (total + (int64_t)threads * kReshapeUnroll - 1) / ((int64_t)threads * kReshapeUnroll);
-    for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
-        const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
-        for (int32_t t = 0; t < nt; t++) {
-            p.dst[t] = cache->base[t0 + t];
-            for (int32_t pl = 0; pl < cache->n_planes; pl++)
-                p.src[t * cache->n_planes + pl] = new_kv[(int64_t)(t0 + t) * cache->n_planes + pl];
-        }
-        // about four waves of 8 resident CTAs per SM over all tensors of the launch
-        const int64_t cap = std::max<int64_t>(1, ((int64_t)dev->num_sms * 8 * 4 + nt - 1) / nt);
-        const dim3 grid((unsigned)std::min(per_tensor_ctas, cap), (unsigned)nt);
-        reshape_and_cache_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(p);
-        st = pkv::cuda_status(cudaGetLastError());
-        if (st != KV_OK) return st;
-    }
-    return KV_OK;
+int kv_write_tokens(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride,
+                    const int32_t *block_table, int32_t n_reqs, int32_t max_blocks_per_req, int64_t bt_row_stride,
+                    const int32_t *token_req, const int32_t *token_pos, int64_t n_tokens, int64_t *slot_out,
+                    kv_stream_t stream)
+{
+    if (n_reqs < 0 || max_blocks_per_req < 0 || bt_row_stride < 0) return KV_ERR_INVALID_ARG;
+    if (n_tokens > 0 && (token_req == nullptr || token_pos == nullptr ||
+                         (n_reqs > 0 && max_blocks_per_req > 0 && block_table == nullptr)))
+        return KV_ERR_INVALID_ARG;
+    if (n_reqs > 0 && bt_row_stride < max_blocks_per_req) return KV_ERR_INVALID_ARG;
+    ReshapeParams p{};
+    p.table = block_table;
+    p.token_req = token_req;
+    p.token_pos = token_pos;
+    p.slot_out = slot_out;
+    p.table_row_stride = bt_row_stride;
+    p.n_reqs = n_reqs;
+    p.max_blocks = max_blocks_per_req;
+    return launch_rows<true>(cache, new_kv, new_token_stride, n_tokens, p, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -26,7 +26,7 @@ RUN_WORDS = 6  # a kv_xfer_run is 24 bytes: six int32 words (the last two hold t
 EXPORTS = ("kv_version", "kv_status_string", "kv_last_cuda_error", "kv_slot_mapping", "kv_reshape_and_cache",
            "kv_xfer_workspace_bytes", "kv_build_xfer_list", "kv_pack_blocks", "kv_unpack_blocks",
            "kv_get_last_error", "kv_build_xfer_list_static", "kv_unpack_blocks_signal", "kv_wait_signal",
-           "kv_clip_block_lists", "kv_block_hashes")
+           "kv_clip_block_lists", "kv_block_hashes", "kv_write_tokens")
 
 
 class KvError(RuntimeError):
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "kv_wait_signal": ([P, ctypes.c_uint64, ctypes.c_uint32, P, P], ctypes.c_int),
             "kv_clip_block_lists": ([P, i32, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
             "kv_block_hashes": ([P, i32, P, i64, i32, ctypes.c_uint64, P, P, i64, P], ctypes.c_int),
+            "kv_write_tokens": ([D, P, i64, P, i32, i32, i64, P, P, i64, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -236,6 +237,22 @@ def kv_reshape_and_cache(cache: PagedCache, new_kv: Sequence[torch.Tensor], slot
     d = cache.desc()
     _check("kv_reshape_and_cache", load().kv_reshape_and_cache(
         ctypes.byref(d), ctypes.cast(ptrs, ctypes.c_void_p), stride, _ptr(slot), slot.shape[0], _stream(stream)))
+
+
+def kv_write_tokens(cache: PagedCache, new_kv: Sequence[torch.Tensor], block_table: torch.Tensor,
+                    token_req: torch.Tensor, token_pos: torch.Tensor, slot_out: Optional[torch.Tensor] = None,
+                    stream=None):
+    """kv_slot_mapping + kv_reshape_and_cache in one launch; slot_out (int64 [T]) optionally gets the slots."""
+    _i32(token_req, "token_req"), _i32(token_pos, "token_pos")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be a row-major int32 [n_reqs, max_blocks] CUDA tensor")
+    new_kv = list(new_kv)
+    stride = new_kv[0].stride(0) * new_kv[0].element_size() if new_kv else cache.row_bytes
+    ptrs = (ctypes.c_uint64 * max(1, len(new_kv)))(*[x.data_ptr() for x in new_kv])
+    _check("kv_write_tokens", load().kv_write_tokens(
+        ctypes.byref(cache.desc()), ctypes.cast(ptrs, ctypes.c_void_p), stride, _ptr(block_table),
+        block_table.shape[0], block_table.shape[1], block_table.stride(0), _ptr(token_req), _ptr(token_pos),
+        token_req.shape[0], _ptr(slot_out), _stream(stream)))
 
 
 def kv_xfer_workspace_bytes(n_blocks: int) -> int:

@@ -94,6 +94,13 @@ class TransferStep:
         K.kv_slot_mapping(self.block_table, self.token_req, self.token_pos, self.src.block_size, self.slot, stream)
         K.kv_reshape_and_cache(self.src, self.new_kv, self.slot, stream)
 
+    def write_tokens_fused(self, stream=None):
+        """The same write as write_tokens with the slot lookup fused into the row copy (one launch)."""
+        if not self.n_tokens:
+            return
+        K.kv_write_tokens(self.src, self.new_kv, self.block_table, self.token_req, self.token_pos, self.slot,
+                          stream)
+
     @staticmethod
     def kept_blocks(case: Case, window: int, block_size: int) -> int:
         """Entries the sliding-window clip keeps, from the host's copy of the per-request

@@ -374,3 +374,48 @@ def test_staging_guard_canaries(wl):
     assert (b[:guard] == 0xA5).all() and (b[guard + n:] == 0xA5).all()
     want = oracle.pack(H.ora_cache(wl.src, src), case.req_offsets, case.src_ids, wl.slice_off, wl.moved_slice)
     np.testing.assert_array_equal(b[guard:guard + n], want)
+
+
+@pytest.mark.parametrize("wl", [W.TINY, W.small(W.MLA), W.small(W.PAGE), W.small(W.PAGE_KV_FIRST)],
+                         ids=lambda w: w.name)
+def test_write_tokens_fused_matches_oracle(wl):
+    """kv_write_tokens (slot lookup fused into the row copy) == oracle slot_mapping + reshape_and_cache."""
+    case = W.make_case(wl)
+    src, _, new = G.host_inputs(wl, case, seed=wl.seed + 17)
+    s_dev = W.to_device_bf16(src, "cuda")
+    n_dev = [x.reshape(G._new_shape(wl.src, case.n_tokens)) for x in W.to_device_bf16(new, "cuda")]
+    cache = K.PagedCache.from_tensors(s_dev, wl.src.layout)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    slot = torch.full((case.n_tokens,), -7, dtype=torch.int64, device="cuda")
+    K.kv_get_last_error(clear=True)
+    K.kv_write_tokens(cache, n_dev, t(case.block_table), t(case.token_req), t(case.token_pos), slot)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() == 0
+    want_slot, bad = oracle.slot_mapping(case.block_table, case.token_req, case.token_pos, wl.src.block_size)
+    assert bad == 0
+    np.testing.assert_array_equal(slot.cpu().numpy(), want_slot)
+    sc = H.ora_cache(wl.src, [a.copy() for a in src])
+    assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], want_slot) == 0
+    for a, b in zip(s_dev, sc.tensors):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+
+
+def test_write_tokens_invalid_tokens():
+    g = W.CacheGeom("separate", 8, 4, 1, 64)
+    host = W.host_cache_tensors(g, 1, np.random.default_rng(2))
+    dev = W.to_device_bf16(host, "cuda")
+    cache = K.PagedCache.from_tensors(dev, "separate")
+    table = torch.tensor([[1, 2], [3, -1]], dtype=torch.int32, device="cuda")
+    req = torch.tensor([0, 1, 1, 5], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([5, 2, 6, 0], dtype=torch.int32, device="cuda")  # 2nd ok, 3rd hits -1, 4th bad req
+    rows = torch.arange(4 * 64, dtype=torch.int16, device="cuda").view(torch.bfloat16).reshape(4, 1, 64)
+    slot = torch.empty(4, dtype=torch.int64, device="cuda")
+    K.kv_write_tokens(cache, [rows], table, req, pos, slot)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() & K.KV_DERR_TABLE
+    np.testing.assert_array_equal(slot.cpu().numpy(), [9, 14, -1, -1])
+    got = dev[0].cpu().view(torch.int16).numpy().reshape(32, 64)
+    want = host[0].view(np.int16).reshape(32, 64).copy()
+    r = rows.view(torch.int16).cpu().numpy().reshape(4, 64)
+    want[9], want[14] = r[0], r[1]
+    np.testing.assert_array_equal(got, want)
