@@ -28,6 +28,7 @@ constexpr int kItems = 8;
 constexpr int kTile = kThreads * kItems;
 constexpr int kWarps = kThreads / 32;
 constexpr int64_t kHeaderBytes = 256;
+constexpr int kOffsetCache = 1024;  // request offsets kept in shared memory when n_reqs + 1 fits
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s bound on any look-back wait
 
 struct TileRecord {  // 32 bytes per tile in the workspace
@@ -104,8 +105,8 @@ struct Sum {
     __device__ int32_t operator()(int32_t a, int32_t b) const { return a + b; }
 };
 
-// Exclusive block-wide scan of one value per thread; *total gets the reduction.
-template <typename Op>
+// Exclusive block-wide scan of one value per thread over NW warps; *total gets the reduction.
+template <int NW = kWarps, typename Op>
 __device__ int32_t block_exclusive(int32_t v, int32_t identity, Op op, int32_t *sh, int32_t *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -117,13 +118,16 @@ __device__ int32_t block_exclusive(int32_t v, int32_t identity, Op op, int32_t *
     }
     if (lane == 31) sh[warp] = incl;
     __syncthreads();
-    int32_t before = identity, all = identity;
+    // every warp scans the NW warp totals itself (one shared load and five shuffles)
+    int32_t w_incl = lane < NW ? sh[lane] : identity;
 #pragma unroll
-    for (int w = 0; w < kWarps; w++) {
-        const int32_t x = sh[w];
-        if (w < warp) before = op(before, x);
-        all = op(all, x);
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, w_incl, d);
+        if (lane >= d) w_incl = op(w_incl, y);
     }
+    const int32_t all = __shfl_sync(0xffffffffu, w_incl, 31);
+    int32_t before = __shfl_sync(0xffffffffu, w_incl, warp > 0 ? warp - 1 : 0);
+    if (warp == 0) before = identity;
     __syncthreads();
     int32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) excl = identity;
@@ -146,6 +150,136 @@ struct XferParams {
     int32_t cap;
 };
 
+// Place of an entry d entries after its run's natural start: d % cap, or d without a cap.
+__device__ __forceinline__ int32_t phase_of(int32_t d, int32_t cap) { return cap > 0 ? d % cap : d; }
+__device__ __forceinline__ int32_t next_phase(int32_t ph, int32_t cap)
+{
+    return (cap > 0 && ph + 1 == cap) ? 0 : ph + 1;
+}
+
+// First half of a tile: stage the tile's ids (one halo entry each side) and, when few, the
+// request offsets in shared memory with coalesced loads; then mark, for this thread's ITEMS
+// entries from i0 and the entry after them, which are natural run starts (request start, or
+// a break in src or dst id contiguity; past the list counts as a start), with each entry's
+// request.  Ends with the block synchronised.
+template <int ITEMS, int NT>
+__device__ __forceinline__ void stage_and_mark(const XferParams &p, int32_t tile_start, int32_t *sh_src,
+                                               int32_t *sh_dst, int32_t *sh_off, bool (&nat)[ITEMS + 1],
+                                               int32_t (&req)[ITEMS])
+{
+    constexpr int kT = ITEMS * NT;
+    const int tid = threadIdx.x;
+    for (int k = tid; k < kT + 2; k += NT) {
+        const int32_t i = tile_start - 1 + k;
+        const bool in = i >= 0 && i < p.n;
+        sh_src[k] = in ? p.src[i] : 0;
+        if (p.dst) sh_dst[k] = in ? p.dst[i] : 0;
+    }
+    const bool off_cached = p.n_reqs + 1 <= kOffsetCache;
+    if (off_cached)
+        for (int k = tid; k <= p.n_reqs; k += NT) sh_off[k] = p.req_offsets[k];
+    __syncthreads();
+    auto offset = [&](int32_t k) { return off_cached ? sh_off[k] : p.req_offsets[k]; };
+
+    const int32_t i0 = tile_start + tid * ITEMS;
+    if (i0 >= p.n) {
+#pragma unroll
+        for (int k = 0; k <= ITEMS; k++) nat[k] = true;
+#pragma unroll
+        for (int k = 0; k < ITEMS; k++) req[k] = 0;
+        return;
+    }
+    int32_t lo = 0, hi = p.n_reqs - 1;  // last request whose first entry is <= i0
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (offset(mid) <= i0) lo = mid;
+        else hi = mid - 1;
+    }
+    int32_t r = lo;
+    int32_t begin = offset(r), end = offset(r + 1);
+    const int32_t base = i0 - tile_start + 1;  // index of entry i0 in the staged ids
+    int32_t prev_s = sh_src[base - 1];
+    int32_t prev_d = p.dst ? sh_dst[base - 1] : 0;
+#pragma unroll
+    for (int k = 0; k <= ITEMS; k++) {
+        const int32_t i = i0 + k;
+        if (i >= p.n) {
+            nat[k] = true;  // past the list: closes the last run
+            if (k < ITEMS) req[k] = r;
+            continue;
+        }
+        while (i >= end && r < p.n_reqs - 1) {
+            r++;
+            begin = end;
+            end = offset(r + 1);
+        }
+        const int32_t sv = sh_src[base + k];
+        const int32_t dv = p.dst ? sh_dst[base + k] : 0;
+        nat[k] = (i == begin) || (sv != prev_s + 1) || (p.dst != nullptr && dv != prev_d + 1);
+        if (k < ITEMS) req[k] = r;
+        prev_s = sv;
+        prev_d = dv;
+    }
+}
+
+// Second half of a tile: with s0, the natural start open at this thread's first entry i0, and
+// cnt0, the runs started before the tile, number every run start and write each run's record
+// at its last entry (the entry whose successor starts a run).  Returns the run starts in the
+// tile.  An entry whose run start is unknown (s0 < 0) sets `unknown_err`.
+template <int ITEMS = kItems, int NW = kWarps>
+__device__ __forceinline__ int32_t resolve_and_write(const XferParams &p, const bool (&nat)[ITEMS + 1],
+                                                     const int32_t (&req)[ITEMS], int32_t i0, int32_t tile_start,
+                                                     int32_t tile_end, int32_t s0, int32_t cnt0,
+                                                     const int32_t *sh_src, const int32_t *sh_dst, int32_t *sh_scan,
+                                                     int unknown_err)
+{
+    int32_t ph[ITEMS];  // (i - s) % cap for each entry's natural start s
+    bool start[ITEMS];
+    bool known = s0 >= 0;
+    int32_t mine = 0;
+    {
+        int32_t q = known ? phase_of(i0 - s0, p.cap) : 0;
+#pragma unroll
+        for (int k = 0; k < ITEMS; k++) {
+            const int32_t i = i0 + k;
+            if (i < tile_end && nat[k]) q = 0;
+            ph[k] = q;
+            start[k] = i < tile_end && (nat[k] || (p.cap > 0 && q == 0));
+            mine += start[k] ? 1 : 0;
+            q = next_phase(q, p.cap);
+        }
+    }
+    int32_t total;
+    const int32_t before = block_exclusive<NW>(mine, 0, Sum(), sh_scan, &total);
+    int32_t run = cnt0 + before - 1;  // index of the run holding the current entry
+#pragma unroll
+    for (int k = 0; k < ITEMS; k++) {
+        const int32_t i = i0 + k;
+        if (i >= tile_end) break;
+        if (start[k]) run++;
+        if (nat[k]) known = true;
+        if (!(nat[k + 1] || (p.cap > 0 && ph[k] + 1 == p.cap))) continue;
+        const int32_t first = i - ph[k];
+        if (!known || first < 0) {
+            pkv::set_error(p.err, unknown_err);
+            continue;
+        }
+        if ((int64_t)run >= p.capacity || run < 0) {
+            pkv::set_error(p.err, KV_DERR_CAPACITY);
+            continue;
+        }
+        kv_xfer_run out;
+        out.req = req[k];
+        const bool staged = first >= tile_start - 1;
+        out.src_block = staged ? sh_src[first - tile_start + 1] : p.src[first];
+        out.dst_block = p.dst ? (staged ? sh_dst[first - tile_start + 1] : p.dst[first]) : -1;
+        out.n_blocks = ph[k] + 1;
+        out.stage_block = first;
+        p.runs[run] = out;
+    }
+    return total;
+}
+
 __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_constant__ XferParams p)
 {
     __shared__ int32_t sh_scan[kWarps];
@@ -163,46 +297,12 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
     if (tile == 0 && tid == 0 && (p.req_offsets[0] != 0 || p.req_offsets[p.n_reqs] != p.n))
         pkv::set_error(p.err, KV_DERR_LIST);
 
-    // ---- natural run starts of this thread's entries (and of the entry after them) ----
+    __shared__ int32_t sh_src[kTile + 2];
+    __shared__ int32_t sh_dst[kTile + 2];
+    __shared__ int32_t sh_off[kOffsetCache];
     bool nat[kItems + 1];
     int32_t req[kItems];
-    if (i0 < p.n) {
-        int32_t lo = 0, hi = p.n_reqs - 1;  // last request whose first entry is <= i0
-        while (lo < hi) {
-            const int32_t mid = (lo + hi + 1) >> 1;
-            if (p.req_offsets[mid] <= i0) lo = mid;
-            else hi = mid - 1;
-        }
-        int32_t r = lo;
-        int32_t begin = p.req_offsets[r], end = p.req_offsets[r + 1];
-        int32_t prev_s = i0 > 0 ? p.src[i0 - 1] : 0;
-        int32_t prev_d = (i0 > 0 && p.dst) ? p.dst[i0 - 1] : 0;
-#pragma unroll
-        for (int k = 0; k <= kItems; k++) {
-            const int32_t i = i0 + k;
-            if (i >= p.n) {
-                nat[k] = true;  // past the list: closes the last run
-                if (k < kItems) req[k] = r;
-                continue;
-            }
-            while (i >= end && r < p.n_reqs - 1) {
-                r++;
-                begin = end;
-                end = p.req_offsets[r + 1];
-            }
-            const int32_t s = p.src[i];
-            const int32_t d = p.dst ? p.dst[i] : 0;
-            nat[k] = (i == begin) || (s != prev_s + 1) || (p.dst != nullptr && d != prev_d + 1);
-            if (k < kItems) req[k] = r;
-            prev_s = s;
-            prev_d = d;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k <= kItems; k++) nat[k] = true;
-#pragma unroll
-        for (int k = 0; k < kItems; k++) req[k] = 0;
-    }
+    stage_and_mark<kItems, kThreads>(p, tile_start, sh_src, sh_dst, sh_off, nat, req);
 
     // ---- tile aggregate from what is decidable locally ----
     int32_t my_last = -1, my_first = 0x7fffffff;
@@ -219,16 +319,22 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
     int32_t tile_first;
     block_exclusive(my_first, 0x7fffffff, Min(), sh_scan, &tile_first);
 
-    int32_t sk[kItems];  // natural start of each entry's run; -1 while it lies left of the tile
+    // Run starts decidable before the look-back: those after a natural start seen in this tile.
+    // ph is the entry's place in its cap piece, (i - s) % cap (or i - s without a cap), kept by
+    // incrementing: one division per thread instead of one per entry.
     int32_t known = 0;
     {
         int32_t s = s_before;
+        int32_t ph = s >= 0 ? phase_of(i0 - s, p.cap) : 0;
 #pragma unroll
         for (int k = 0; k < kItems; k++) {
             const int32_t i = i0 + k;
-            if (i < tile_end && nat[k]) s = i;
-            sk[k] = s;
-            if (i < tile_end && s >= 0 && (nat[k] || (p.cap > 0 && (i - s) % p.cap == 0))) known++;
+            if (i < tile_end && nat[k]) {
+                s = i;
+                ph = 0;
+            }
+            if (i < tile_end && s >= 0 && (nat[k] || (p.cap > 0 && ph == 0))) known++;
+            ph = next_phase(ph, p.cap);
         }
     }
     int32_t tile_cnt;
@@ -285,42 +391,78 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
     const Pre excl = sh_pre;
 
     // ---- resolve every entry, number the runs, write each run at its last entry ----
-    bool start[kItems];
-    int32_t mine = 0;
+    const int32_t s0 = s_before >= 0 ? s_before : excl.s;  // -1 only after a look-back timeout
+    resolve_and_write(p, nat, req, i0, tile_start, tile_end, s0, excl.cnt, sh_src, sh_dst, sh_scan,
+                      KV_DERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// Single-CTA builder for lists that fit one tile of kSTile entries: the look-back kernel
+// without the look-back, so it needs neither the scratch nor its zeroing.  A short list
+// (a decode-side request, a few prompts) is then one launch.  Longer lists go to the
+// look-back kernel: one CTA walking several tiles in turn is slower than one CTA per tile.
+// ---------------------------------------------------------------------------
+constexpr int kSThreads = 1024;
+constexpr int kSItems = 4;
+constexpr int kSTile = kSThreads * kSItems;
+constexpr int kSWarps = kSThreads / 32;
+
+__global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __grid_constant__ XferParams p)
+{
+    __shared__ int32_t sh_src[kSTile + 2];
+    __shared__ int32_t sh_dst[kSTile + 2];
+    __shared__ int32_t sh_off[kOffsetCache];
+    __shared__ int32_t sh_scan[kSWarps];
+
+    const int tid = threadIdx.x;
+    if (tid == 0 && (p.req_offsets[0] != 0 || p.req_offsets[p.n_reqs] != p.n)) pkv::set_error(p.err, KV_DERR_LIST);
+    bool nat[kSItems + 1];
+    int32_t req[kSItems];
+    stage_and_mark<kSItems, kSThreads>(p, 0, sh_src, sh_dst, sh_off, nat, req);
+    const int32_t i0 = tid * kSItems;
+    int32_t my_last = -1;
 #pragma unroll
-    for (int k = 0; k < kItems; k++) {
-        const int32_t i = i0 + k;
-        if (sk[k] < 0) sk[k] = excl.s;
-        start[k] = i < tile_end && (nat[k] || (p.cap > 0 && (i - sk[k]) % p.cap == 0));
-        mine += start[k] ? 1 : 0;
-    }
+    for (int k = 0; k < kSItems; k++)
+        if (i0 + k < p.n && nat[k]) my_last = i0 + k;
     int32_t unused;
-    const int32_t before = block_exclusive(mine, 0, Sum(), sh_scan, &unused);
-    int32_t run = excl.cnt + before - 1;  // index of the run holding the current entry
-#pragma unroll
-    for (int k = 0; k < kItems; k++) {
-        const int32_t i = i0 + k;
-        if (i >= tile_end) break;
-        if (start[k]) run++;
-        const bool next_starts = nat[k + 1] || (p.cap > 0 && (i + 1 - sk[k]) % p.cap == 0);
-        if (!next_starts) continue;
-        const int32_t first = p.cap > 0 ? sk[k] + ((i - sk[k]) / p.cap) * p.cap : sk[k];
-        if (first < 0 || first > i) {  // only after a look-back timeout
-            pkv::set_error(p.err, KV_DERR_TIMEOUT);
-            continue;
-        }
-        if ((int64_t)run >= p.capacity || run < 0) {
-            pkv::set_error(p.err, KV_DERR_CAPACITY);
-            continue;
-        }
-        kv_xfer_run out;
-        out.req = req[k];
-        out.src_block = p.src[first];
-        out.dst_block = p.dst ? p.dst[first] : -1;
-        out.n_blocks = i - first + 1;
-        out.stage_block = first;
-        p.runs[run] = out;
+    // natural start open at i0; -1 only when the offsets do not start at 0
+    const int32_t s0 = block_exclusive<kSWarps>(my_last, -1, Max(), sh_scan, &unused);
+    const int32_t cnt = resolve_and_write<kSItems, kSWarps>(p, nat, req, i0, 0, p.n, s0, 0, sh_src, sh_dst, sh_scan,
+                                                            KV_DERR_LIST);
+    if (tid == 0) {
+        *p.n_runs = cnt;
+        if ((int64_t)cnt > p.capacity) pkv::set_error(p.err, KV_DERR_CAPACITY);
     }
+}
+
+// Launches the single-CTA builder for lists of one tile (the scratch is not touched), else zeroes the look-back scratch (tile counter and tile records: `need` bytes
+// at `scratch`) and launches one CTA per tile.
+int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *src_ids, const int32_t *dst_ids,
+                   int64_t n_blocks, int32_t max_run_blocks, kv_xfer_run *runs, int64_t run_capacity,
+                   int32_t *n_runs, void *scratch, int64_t need, const pkv::DeviceInfo &dev, cudaStream_t s)
+{
+    XferParams p{};
+    p.req_offsets = req_offsets;
+    p.src = src_ids;
+    p.dst = dst_ids;
+    p.runs = runs;
+    p.n_runs = n_runs;
+    p.err = dev.err_word;
+    p.capacity = run_capacity;
+    p.n_reqs = n_reqs;
+    p.n = (int32_t)n_blocks;
+    p.cap = max_run_blocks;
+    if (n_blocks <= kSTile) {
+        build_xfer_single_kernel<<<1, kSThreads, 0, s>>>(p);
+        return pkv::cuda_status(cudaGetLastError());
+    }
+    const int st = pkv::cuda_status(cudaMemsetAsync(scratch, 0, (size_t)need, s));
+    if (st != KV_OK) return st;
+    p.counter = reinterpret_cast<uint32_t *>(scratch);
+    p.tiles = reinterpret_cast<TileRecord *>(reinterpret_cast<uint8_t *>(scratch) + kHeaderBytes);
+    const int tiles = (int)((n_blocks + kTile - 1) / kTile);
+    build_xfer_kernel<<<tiles, kThreads, 0, s>>>(p);
+    return pkv::cuda_status(cudaGetLastError());
 }
 
 }  // namespace
@@ -356,25 +498,8 @@ int kv_build_xfer_list(const int32_t *req_offsets, int32_t n_reqs, const int32_t
     if (((uintptr_t)runs & 7u) != 0) return KV_ERR_ALIGN;
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
-
-    int st = pkv::cuda_status(cudaMemsetAsync(workspace, 0, (size_t)need, s));
-    if (st != KV_OK) return st;
-    XferParams p{};
-    p.req_offsets = req_offsets;
-    p.src = src_ids;
-    p.dst = dst_ids;
-    p.runs = runs;
-    p.n_runs = n_runs;
-    p.counter = reinterpret_cast<uint32_t *>(workspace);
-    p.tiles = reinterpret_cast<TileRecord *>(reinterpret_cast<uint8_t *>(workspace) + kHeaderBytes);
-    p.err = dev->err_word;
-    p.capacity = run_capacity;
-    p.n_reqs = n_reqs;
-    p.n = (int32_t)n_blocks;
-    p.cap = max_run_blocks;
-    const int tiles = (int)((n_blocks + kTile - 1) / kTile);
-    build_xfer_kernel<<<tiles, kThreads, 0, s>>>(p);
-    return pkv::cuda_status(cudaGetLastError());
+    return launch_builder(req_offsets, n_reqs, src_ids, dst_ids, n_blocks, max_run_blocks, runs, run_capacity,
+                          n_runs, workspace, need, *dev, s);
 }
 
 }  // extern "C"
@@ -442,23 +567,6 @@ extern "C" int kv_build_xfer_list_static(const int32_t *req_offsets, int32_t n_r
 
     int64_t need = 0;
     kv_xfer_workspace_bytes(n_blocks, &need);
-    // the tile counter and the tile records must start at zero; the array keeps the last call's contents
-    st = pkv::cuda_status(cudaMemsetAsync(scratch, 0, (size_t)need, s));
-    if (st != KV_OK) return st;
-    XferParams p{};
-    p.req_offsets = req_offsets;
-    p.src = src_ids;
-    p.dst = dst_ids;
-    p.runs = runs;
-    p.n_runs = n_runs;
-    p.counter = reinterpret_cast<uint32_t *>(scratch);
-    p.tiles = reinterpret_cast<TileRecord *>(reinterpret_cast<uint8_t *>(scratch) + kHeaderBytes);
-    p.err = dev->err_word;
-    p.capacity = run_capacity;
-    p.n_reqs = n_reqs;
-    p.n = (int32_t)n_blocks;
-    p.cap = max_run_blocks;
-    const int tiles = (int)((n_blocks + kTile - 1) / kTile);
-    build_xfer_kernel<<<tiles, kThreads, 0, s>>>(p);
-    return pkv::cuda_status(cudaGetLastError());
+    return launch_builder(req_offsets, n_reqs, src_ids, dst_ids, n_blocks, max_run_blocks, runs, run_capacity,
+                          n_runs, scratch, need, *dev, s);
 }

@@ -58,10 +58,13 @@ def _builder_case(n_reqs, lens, rng, frag=(12, 0.6), n_ids=None):
     return W.csr(W.pop_lists(q, lens))
 
 
-@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096, 6145, 20000, 100003])
+@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4095, 4096, 4097, 6145, 20000, 100003])
 @pytest.mark.parametrize("cap", [0, 1, 2, 7, 32])
 def test_builder_tiles(n, cap):
-    """Runs across tile boundaries, long runs, empty requests, all cap variants."""
+    """Runs across tile boundaries, long runs, empty requests, all cap variants.
+
+    Lists of up to 4096 entries go to the single-CTA builder (one tile), longer ones to the
+    look-back builder (tiles of 2048); the sizes straddle both limits and the look-back tile edges."""
     rng = np.random.default_rng(n * 31 + cap)
     lens = []
     left = n
@@ -103,9 +106,10 @@ def test_builder_empty_and_capacity():
     assert K.kv_get_last_error() & K.KV_DERR_CAPACITY
 
 
-def test_builder_bad_offsets_flagged():
-    o = torch.tensor([0, 3, 5], dtype=torch.int32, device="cuda")  # claims 5 entries, list has 4
-    s = torch.tensor([1, 2, 3, 4], dtype=torch.int32, device="cuda")
+@pytest.mark.parametrize("n", [4, 70000])
+def test_builder_bad_offsets_flagged(n):
+    o = torch.tensor([0, 3, n + 1], dtype=torch.int32, device="cuda")  # claims n + 1 entries, list has n
+    s = torch.arange(1, n + 1, dtype=torch.int32, device="cuda")
     K.kv_build_xfer_list(o, s)
     torch.cuda.synchronize()
     assert K.kv_get_last_error() & K.KV_DERR_LIST

@@ -4,7 +4,7 @@ Some callers cannot allocate device memory when they build a transfer list: a
 transport's progress thread (cudaMalloc / cudaFree may synchronise the device and
 stall the model's stream) or a serving process whose KV-cache pool already took
 nearly all free device memory.  This entry point keeps its scratch in a fixed array
-inside the library.  The test calls it through the C ABI twice in a row, on two
+inside the library.  The test calls it through the C ABI four times in a row, on
 different lists, and checks each result bit-exactly against kv_build_xfer_list
 (the workspace variant) on the same input.  It also checks the size limit.
 
@@ -53,10 +53,11 @@ def _host(x: K.XferList):
 
 
 def test_static_builder_matches_workspace_builder_twice():
-    cases = [(_lists(1, 9000, 17), 2), (_lists(2, 4608, 3), 0)]  # two different lists
+    # different lists; those longer than 4096 entries take the look-back builder, which uses the scratch
+    cases = [(_lists(1, 9000, 17), 2), (_lists(2, 100000, 3), 0), (_lists(3, 3000, 4), 1), (_lists(4, 70001, 5), 7)]
     dev = [tuple(torch.from_numpy(a).cuda() for a in lists) + (cap,) for lists, cap in cases]
     want = [_host(K.kv_build_xfer_list(o, s, d, cap)) for o, s, d, cap in dev]
-    # two calls in a row on one stream: the second reuses the scratch the first left behind
+    # calls in a row on one stream: each look-back call reuses the scratch the one before left behind
     got = [K.kv_build_xfer_list_static(o, s, d, cap) for o, s, d, cap in dev]
     torch.cuda.synchronize()
     for (wc, wr), g in zip(want, got):
