@@ -31,6 +31,10 @@ def test_bench_json_line():
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    ac = d["cpu_baseline_all_cores"]
+    assert ac["kind"] == "oracle" and ac["cores"] >= 1 and ac["value"] > 0
+    for name, k in d["kernels"].items():
+        assert k["ms_best"] <= k["ms_median"] and k["ms_best"] <= k["ms"], name
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 5 * 5  # slot_mapping, reshape_and_cache, builder, pack, unpack per step
