@@ -440,18 +440,25 @@ def measure_prefix_hash(step, dev, stream, reps: int = 20) -> dict:
     toks = torch.from_numpy(rng.integers(0, 128000, size=int(off[-1])).astype(np.int32)).to(dev)
     off_d = torch.from_numpy(off).to(dev)
     bs = case.wl.src.block_size
-    o, h = K.kv_block_hashes(off_d, toks, bs, 81)
+    ws = torch.empty(max(16, K.kv_block_hashes_workspace_bytes(toks.shape[0], bs)), dtype=torch.uint8, device=dev)
+    o, h = K.kv_block_hashes(off_d, toks, bs, 81, workspace=ws)
     torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        K.kv_block_hashes(off_d, toks, bs, 81, o, h)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    us = a.elapsed_time(b) / reps * 1e3
+
+    def timed(workspace):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        K.kv_block_hashes(off_d, toks, bs, 81, o, h, workspace=workspace)
+        a.record(stream)
+        for _ in range(reps):
+            K.kv_block_hashes(off_d, toks, bs, 81, o, h, workspace=workspace)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps * 1e3
+
+    us, chain_us = timed(ws), timed(None)
     n_hashes = int(sum(int(l) // bs for l in lens))
     return {"requests": int(lens.shape[0]), "tokens": int(off[-1]), "hashes": n_hashes, "us": round(us, 2),
-            "hashes_per_s": round(n_hashes / (us * 1e-6), 1)}
+            "hashes_per_s": round(n_hashes / (us * 1e-6), 1), "chain_us": round(chain_us, 2),
+            "note": "us: table split with a workspace (3 launches); chain_us: one thread per request, no workspace"}
 
 
 def measure_single_request(step, dev, blocks: int = 64, iters: int = 200):

@@ -26,7 +26,7 @@ RUN_WORDS = 6  # a kv_xfer_run is 24 bytes: six int32 words (the last two hold t
 EXPORTS = ("kv_version", "kv_status_string", "kv_last_cuda_error", "kv_slot_mapping", "kv_reshape_and_cache",
            "kv_xfer_workspace_bytes", "kv_build_xfer_list", "kv_pack_blocks", "kv_unpack_blocks",
            "kv_get_last_error", "kv_build_xfer_list_static", "kv_unpack_blocks_signal", "kv_wait_signal",
-           "kv_clip_block_lists", "kv_block_hashes", "kv_write_tokens")
+           "kv_clip_block_lists", "kv_block_hashes", "kv_block_hashes_workspace_bytes", "kv_write_tokens")
 
 
 class KvError(RuntimeError):
@@ -91,7 +91,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.c_int),
             "kv_wait_signal": ([P, ctypes.c_uint64, ctypes.c_uint32, P, P], ctypes.c_int),
             "kv_clip_block_lists": ([P, i32, P, i64, P, i32, i32, P, P, i64, P], ctypes.c_int),
-            "kv_block_hashes": ([P, i32, P, i64, i32, ctypes.c_uint64, P, P, i64, P], ctypes.c_int),
+            "kv_block_hashes": ([P, i32, P, i64, i32, ctypes.c_uint64, P, P, i64, P, i64, P], ctypes.c_int),
+            "kv_block_hashes_workspace_bytes": ([i64, i32, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "kv_write_tokens": ([D, P, i64, P, i32, i32, i64, P, P, i64, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
@@ -322,20 +323,37 @@ def kv_clip_block_lists(req_offsets: torch.Tensor, ids: torch.Tensor, n_tokens: 
     return out_offsets, out_ids
 
 
+def kv_block_hashes_workspace_bytes(n_tokens: int, block_size: int) -> int:
+    out = ctypes.c_int64(0)
+    _check("kv_block_hashes_workspace_bytes", load().kv_block_hashes_workspace_bytes(int(n_tokens), int(block_size),
+                                                                                     ctypes.byref(out)))
+    return out.value
+
+
 def kv_block_hashes(tok_offsets: torch.Tensor, tokens: torch.Tensor, block_size: int, seed: int,
                     out_offsets: Optional[torch.Tensor] = None, out_hashes: Optional[torch.Tensor] = None,
-                    stream=None):
+                    workspace="auto", stream=None):
     """Prefix hash chain of every request's full token blocks; returns device (out_offsets int32,
-    out_hashes int64 holding the uint64 bit patterns)."""
+    out_hashes int64 holding the uint64 bit patterns).  workspace: "auto" (a uint8 device tensor
+    of kv_block_hashes_workspace_bytes is allocated here, for the table path), None (the plain
+    per-request chain) or a caller's uint8 tensor."""
     _i32(tok_offsets, "tok_offsets"), _i32(tokens, "tokens")
     cap = max(1, tokens.shape[0] // int(block_size))
     if out_offsets is None:
         out_offsets = torch.empty_like(tok_offsets)
     if out_hashes is None:
         out_hashes = torch.empty(cap, dtype=torch.int64, device=tokens.device)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError(f"workspace must be 'auto', None or a tensor, not {workspace!r}")
+        need = kv_block_hashes_workspace_bytes(tokens.shape[0], block_size)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=tokens.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("kv_block_hashes", load().kv_block_hashes(
         _ptr(tok_offsets), tok_offsets.shape[0] - 1, _ptr(tokens), tokens.shape[0], int(block_size),
-        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_offsets), _ptr(out_hashes), out_hashes.shape[0], _stream(stream)))
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_offsets), _ptr(out_hashes), out_hashes.shape[0], ws_ptr, ws_bytes,
+        _stream(stream)))
     return out_offsets, out_hashes
 
 

@@ -138,3 +138,13 @@ int main() {
                        check=True)
         r = subprocess.run([os.path.join(d, "t")], capture_output=True, text=True)
         assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout
+
+
+def test_hash_workspace_size(lib):
+    out = ctypes.c_int64(-1)
+    assert lib.kv_block_hashes_workspace_bytes(73728, 16, ctypes.byref(out)) == K.KV_OK
+    assert out.value == 4608 * 256 * 8  # one 256-entry table of 8-byte sums per full block
+    assert lib.kv_block_hashes_workspace_bytes(15, 16, ctypes.byref(out)) == K.KV_OK and out.value == 0
+    assert lib.kv_block_hashes_workspace_bytes(16, 0, ctypes.byref(out)) == K.KV_ERR_INVALID_ARG
+    assert lib.kv_block_hashes_workspace_bytes(-1, 16, ctypes.byref(out)) == K.KV_ERR_INVALID_ARG
+    assert lib.kv_block_hashes_workspace_bytes(16, 16, None) == K.KV_ERR_INVALID_ARG
