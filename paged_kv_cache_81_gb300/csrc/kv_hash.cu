@@ -165,8 +165,53 @@ constexpr int kTableChunk = 512;    // tokens staged in shared memory at a time
 #endif
 constexpr int kRing = PKV_HASH_RING;  // tables in flight per walking warp
 
+// 64-bit arithmetic modulo 2^64 for the table weights.
+__host__ __device__ constexpr uint64_t pow_mod_2_64(uint64_t base, uint64_t e)
+{
+    uint64_t r = 1;
+    while (e) {
+        if (e & 1) r *= base;
+        base *= base;
+        e >>= 1;
+    }
+    return r;
+}
+__host__ __device__ constexpr uint64_t inverse_mod_2_64(uint64_t odd)
+{
+    uint64_t x = odd;  // correct to 3 bits; each Newton step doubles that
+    for (int i = 0; i < 5; i++) x *= 2 - odd * x;
+    return x;
+}
+constexpr uint64_t kPrimeInvPow256 = pow_mod_2_64(inverse_mod_2_64(kFnvPrime), kTableThreads);
+static_assert(kFnvPrime * inverse_mod_2_64(kFnvPrime) == 1, "P is odd, so invertible modulo 2^64");
+
+// A weight W split for two 32-bit multiply-adds per byte: lo_s is W's low word read as signed,
+// hi = W's high word plus bit 31 of the low word, so that for any 32-bit signed d
+//     d * W = d * lo_s + 2^32 * (d * hi)   (mod 2^64).
+struct SplitWeight {
+    int32_t lo_s;
+    uint32_t hi;
+};
+__device__ __forceinline__ SplitWeight split_weight(uint64_t w)
+{
+    const uint32_t lo = (uint32_t)w;
+    return SplitWeight{(int32_t)lo, (uint32_t)(w >> 32) + (lo >> 31)};
+}
+__device__ __forceinline__ uint64_t join_weight(SplitWeight s)
+{
+    const uint32_t lo = (uint32_t)s.lo_s;
+    return ((uint64_t)(s.hi - (lo >> 31)) << 32) | lo;
+}
+
 // Block g's table: D[c] for c = threadIdx.x.  Blocks are numbered by their hash index; a CTA
 // takes blocks g = blockIdx.x, + gridDim.x, ... below min(hash count, limit).
+// D = sum_k P^(n-k) d_k is taken as a weighted sum over the block's bytes in chunks of at most
+// kTableChunkBytes, joined by Horner (D <- D * P^(chunk bytes) + chunk sum).  The weights
+// P^(M - i), M = min(n, kTableChunkBytes), are computed once per CTA into shared memory; a
+// chunk of m bytes uses the last m of them.  Per byte: a byte extract and xor, one
+// subtraction, a signed 32x32->64 multiply-add, a 32-bit multiply-add, and the chain's multiply.
+constexpr int kTableChunkBytes = 4 * kTableChunk;
+
 __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
                                                                    const int32_t *__restrict__ tokens,
                                                                    int32_t n_tokens, int32_t bs,
@@ -174,8 +219,18 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
                                                                    uint64_t *__restrict__ table, int64_t limit)
 {
     __shared__ uint32_t sh_tok[kTableChunk];
+    __shared__ SplitWeight sh_w[kTableChunkBytes];
     const int64_t n_hash = min((int64_t)out_off[n_reqs], limit);
     const uint32_t c0 = threadIdx.x;
+    const int32_t nb = 4 * bs;  // token bytes per block
+    const int32_t M = min(nb, kTableChunkBytes);
+    if ((int32_t)c0 < M) {
+        uint64_t w = pow_mod_2_64(kFnvPrime, (uint64_t)(M - (int32_t)c0));
+        for (int32_t i = c0; i < M; i += kTableThreads) {
+            sh_w[i] = split_weight(w);  // P^(M - i)
+            w *= kPrimeInvPow256;       // P^(M - i - 256)
+        }
+    }
     for (int64_t g = blockIdx.x; g < n_hash; g += gridDim.x) {
         int32_t lo = 0, hi = n_reqs - 1;  // the request holding hash g: last r with out_off[r] <= g
         while (lo < hi) {
@@ -190,18 +245,28 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
         uint64_t D = 0;
         for (int32_t j0 = 0; j0 < bs; j0 += kTableChunk) {
             const int32_t m = min(kTableChunk, bs - j0);
-            __syncthreads();  // the previous chunk has been read
+            const SplitWeight *w = sh_w + (M - 4 * m);
+            __syncthreads();  // the previous chunk has been read (and, the first time, the weights written)
             for (int q = threadIdx.x; q < m; q += kTableThreads) sh_tok[q] = ok ? (uint32_t)tokens[first + j0 + q] : 0u;
             __syncthreads();
+            int64_t acc = 0;
+            uint32_t acc_hi = 0;
+            // c keeps the product's high bits: x and c then share all but their low byte, so
+            // x - c is still the low bytes' difference, and x's low byte alone sets c's next one.
+#pragma unroll 2
             for (int q = 0; q < m; q++) {
                 const uint32_t v = sh_tok[q];
 #pragma unroll
                 for (int byte = 0; byte < 4; byte++) {
                     const uint32_t x = c ^ ((v >> (8 * byte)) & 0xffu);
-                    D = (D + (uint64_t)(int64_t)((int32_t)x - (int32_t)c)) * kFnvPrime;
-                    c = (x * 0x1b3u) & 0xffu;
+                    const int32_t d = (int32_t)x - (int32_t)c;
+                    const SplitWeight wk = w[4 * q + byte];
+                    acc += (int64_t)d * wk.lo_s;
+                    acc_hi += (uint32_t)d * wk.hi;
+                    c = x * 0x1b3u;
                 }
             }
+            D = D * join_weight(w[0]) + (uint64_t)acc + ((uint64_t)acc_hi << 32);
         }
         table[g * 256 + c0] = D;
     }
@@ -271,21 +336,6 @@ __global__ void __launch_bounds__(32) hash_walk_kernel(const int32_t *__restrict
         cp_async_wait<0>();
         __syncwarp();
     }
-}
-
-}  // namespace
-
-namespace {
-
-uint64_t pow_mod_2_64(uint64_t base, uint64_t e)
-{
-    uint64_t r = 1;
-    while (e) {
-        if (e & 1) r *= base;
-        base *= base;
-        e >>= 1;
-    }
-    return r;
 }
 
 }  // namespace
