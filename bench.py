@@ -59,6 +59,8 @@ def parse():
                     help="clip every request's block lists to the last N tokens before the xfer_list (0 = off)")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling captures)")
     ap.add_argument("--num-blocks", type=int, default=None, help="override blocks per tensor (profiling captures)")
+    ap.add_argument("--hash-only", action="store_true",
+                    help="run only the prefix-hash measurement (kv_block_hashes), e.g. to profile its kernels")
     return ap.parse_args()
 
 
@@ -319,7 +321,7 @@ def run_ours(args):
     write_path = measure_write_path(step, dev) if extras and step.n_tokens else None
     prior_art = measure_prior_art(step, dev, stream) if extras and args.stage == "device" and not args.sw_window \
         else None
-    prefix_hash = measure_prefix_hash(step, dev, stream) if extras and case.req_tokens is not None else None
+    prefix_hash = measure_prefix_hash(case, dev, stream) if extras and case.req_tokens is not None else None
     single = measure_single_request(step, dev) if extras and args.stage == "device" and not args.sw_window else None
 
     host_link = None
@@ -428,12 +430,11 @@ def measure_prior_art(step, dev, stream, reps: int = 5):
     return out
 
 
-def measure_prefix_hash(step, dev, stream, reps: int = 20) -> dict:
+def measure_prefix_hash(case, dev, stream, reps: int = 20) -> dict:
     """kv_block_hashes over the batch's token ids (seeded synthetic ids, the case's request lengths)."""
     import torch
     from paged_kv_cache_81_gb300 import pagedkv as K
 
-    case = step.case
     rng = np.random.default_rng(case.wl.seed + 7)
     lens = case.req_tokens.astype(np.int64)
     off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -793,9 +794,27 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_hash_only(args):
+    """Only the prefix-hash measurement of the workload's batch (no caches are allocated): the
+    driver for profiling the hash kernels."""
+    import torch
+    from paged_kv_cache_81_gb300 import build
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workload(args)
+    case = W.make_case(wl)
+    if case.req_tokens is None:
+        raise SystemExit(f"workload {wl.name} has no token batch to hash")
+    print(json.dumps({"workload": wl.name, "prefix_hash": measure_prefix_hash(case, dev, torch.cuda.current_stream(dev),
+                                                                             reps=args.steps)}), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.hash_only:
+        run_hash_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
