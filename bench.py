@@ -582,6 +582,10 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
     n_runs_host = torch.empty(steps, dtype=torch.int32, pin_memory=True)
     copied = [torch.cuda.Event() for _ in range(2)]
     freed = [torch.cuda.Event() for _ in range(2)]
+    # per-step copy brackets on the copy stream: the rate the link delivers while the steps run
+    c_begin = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    c_end = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    timing = {"on": False}
     h2d = sum(h.numel() * h.element_size() for h in host.values()) + (
         host_rows.numel() * host_rows.element_size() if host_rows is not None else 0)
     d2h = 4
@@ -590,11 +594,15 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
         b = k % 2
         if k >= 2:
             copy_stream.wait_event(freed[b])  # step k-2 is done with this buffer set
+        if timing["on"]:
+            c_begin[k].record(copy_stream)
         with torch.cuda.stream(copy_stream):
             for n in names:
                 sets[b][n].copy_(host[n], non_blocking=True)
             if host_rows is not None:
                 sets[b]["_rows"].copy_(host_rows, non_blocking=True)
+        if timing["on"]:
+            c_end[k].record(copy_stream)
         copied[b].record(copy_stream)
 
     def run_step(k):
@@ -621,11 +629,14 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
+    timing["on"] = True
     t0 = time.perf_counter()
     run(steps)
     err = K.kv_get_last_error(clear=False)  # 4-byte read of the device error word; synchronises
     barrier()
     secs = time.perf_counter() - t0
+    timing["on"] = False
+    copy_ms = sum(c_begin[k].elapsed_time(c_end[k]) for k in range(steps))
     if err:
         raise RuntimeError(f"device error word {err:#x} in the end-to-end run")
     for n in names:  # leave the step on its original buffers
@@ -642,6 +653,9 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
         link = measure_host_link(host_rows.view(torch.uint8).reshape(-1), dev, comp, reps=3)["h2d_gbs"]
         out["h2d_link_gbs"] = link
         out["link_bound_ms_per_step"] = round(h2d / (link * 1e9) * 1e3, 4)
+    # what the copies achieved inside the timed run (the link is shared with the host's other work)
+    out["h2d_gbs_during_run"] = round(h2d * steps / (copy_ms * 1e-3) / 1e9, 1)
+    out["copy_ms_per_step_during_run"] = round(copy_ms / steps, 4)
     return out
 
 
