@@ -201,7 +201,7 @@ KV_API int kv_xfer_workspace_bytes(int64_t n_blocks, int64_t *bytes_out);
  * set and only the first run_capacity runs are written; n_blocks runs always suffice).
  * workspace: device scratch of kv_xfer_workspace_bytes(n_blocks) bytes, 16-byte
  * aligned, zeroed by this call on `stream`; calls sharing a workspace must be ordered.
- * Lists of up to 4096 entries are built by one CTA that leaves the workspace untouched
+ * Lists of up to 5120 entries are built by one CTA that leaves the workspace untouched
  * (it must still be passed and large enough).
  * Limit: n_blocks < 2^31 - 2^12.
  */

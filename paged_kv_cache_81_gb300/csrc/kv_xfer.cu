@@ -168,16 +168,44 @@ __device__ __forceinline__ void stage_and_mark(const XferParams &p, int32_t tile
                                                int32_t (&req)[ITEMS])
 {
     constexpr int kT = ITEMS * NT;
+    constexpr int kPer = (kT + 2 + NT - 1) / NT;  // staged ids per thread
     const int tid = threadIdx.x;
-    for (int k = tid; k < kT + 2; k += NT) {
+    // every load is issued before the first shared store: read-only global loads cannot alias
+    // the shared arrays, so they overlap instead of each waiting out the previous store
+    int32_t vs[kPer], vd[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; u++) {
+        const int k = tid + u * NT;
         const int32_t i = tile_start - 1 + k;
-        const bool in = i >= 0 && i < p.n;
-        sh_src[k] = in ? p.src[i] : 0;
-        if (p.dst) sh_dst[k] = in ? p.dst[i] : 0;
+        const bool in = k < kT + 2 && i >= 0 && i < p.n;
+        vs[u] = in ? __ldg(p.src + i) : 0;
+        vd[u] = in && p.dst ? __ldg(p.dst + i) : 0;
     }
     const bool off_cached = p.n_reqs + 1 <= kOffsetCache;
-    if (off_cached)
-        for (int k = tid; k <= p.n_reqs; k += NT) sh_off[k] = p.req_offsets[k];
+    constexpr int kOffPer = (kOffsetCache + NT - 1) / NT;
+    int32_t vo[kOffPer];
+    if (off_cached) {
+#pragma unroll
+        for (int u = 0; u < kOffPer; u++) {
+            const int k = tid + u * NT;
+            vo[u] = k <= p.n_reqs ? __ldg(p.req_offsets + k) : 0;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; u++) {
+        const int k = tid + u * NT;
+        if (k < kT + 2) {
+            sh_src[k] = vs[u];
+            if (p.dst) sh_dst[k] = vd[u];
+        }
+    }
+    if (off_cached) {
+#pragma unroll
+        for (int u = 0; u < kOffPer; u++) {
+            const int k = tid + u * NT;
+            if (k <= p.n_reqs) sh_off[k] = vo[u];
+        }
+    }
     __syncthreads();
     auto offset = [&](int32_t k) { return off_cached ? sh_off[k] : p.req_offsets[k]; };
 
@@ -231,7 +259,7 @@ __device__ __forceinline__ int32_t resolve_and_write(const XferParams &p, const 
                                                      const int32_t (&req)[ITEMS], int32_t i0, int32_t tile_start,
                                                      int32_t tile_end, int32_t s0, int32_t cnt0,
                                                      const int32_t *sh_src, const int32_t *sh_dst, int32_t *sh_scan,
-                                                     int unknown_err)
+                                                     int unknown_err, kv_xfer_run *sh_rec = nullptr)
 {
     int32_t ph[ITEMS];  // (i - s) % cap for each entry's natural start s
     bool start[ITEMS];
@@ -275,7 +303,8 @@ __device__ __forceinline__ int32_t resolve_and_write(const XferParams &p, const 
         out.dst_block = p.dst ? (staged ? sh_dst[first - tile_start + 1] : p.dst[first]) : -1;
         out.n_blocks = ph[k] + 1;
         out.stage_block = first;
-        p.runs[run] = out;
+        if (sh_rec != nullptr) sh_rec[run - cnt0] = out;  // the caller copies the tile's records out
+        else p.runs[run] = out;
     }
     return total;
 }
@@ -294,8 +323,9 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
     const int32_t tile_end = min(tile_start + kTile, p.n);
     const int32_t i0 = tile_start + tid * kItems;
 
-    if (tile == 0 && tid == 0 && (p.req_offsets[0] != 0 || p.req_offsets[p.n_reqs] != p.n))
-        pkv::set_error(p.err, KV_DERR_LIST);
+    const bool checker = tile == 0 && tid == 0;  // validates the offsets' ends, loads issued early
+    const int32_t o_first = checker ? __ldg(p.req_offsets) : 0;
+    const int32_t o_last = checker ? __ldg(p.req_offsets + p.n_reqs) : p.n;
 
     __shared__ int32_t sh_src[kTile + 2];
     __shared__ int32_t sh_dst[kTile + 2];
@@ -303,6 +333,7 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
     bool nat[kItems + 1];
     int32_t req[kItems];
     stage_and_mark<kItems, kThreads>(p, tile_start, sh_src, sh_dst, sh_off, nat, req);
+    if (o_first != 0 || o_last != p.n) pkv::set_error(p.err, KV_DERR_LIST);
 
     // ---- tile aggregate from what is decidable locally ----
     int32_t my_last = -1, my_first = 0x7fffffff;
@@ -402,8 +433,11 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
 // (a decode-side request, a few prompts) is then one launch.  Longer lists go to the
 // look-back kernel: one CTA walking several tiles in turn is slower than one CTA per tile.
 // ---------------------------------------------------------------------------
+#ifndef PKV_XFER_SINGLE_ITEMS
+#define PKV_XFER_SINGLE_ITEMS 5
+#endif
 constexpr int kSThreads = 1024;
-constexpr int kSItems = 4;
+constexpr int kSItems = PKV_XFER_SINGLE_ITEMS;
 constexpr int kSTile = kSThreads * kSItems;
 constexpr int kSWarps = kSThreads / 32;
 
@@ -415,10 +449,12 @@ __global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __gr
     __shared__ int32_t sh_scan[kSWarps];
 
     const int tid = threadIdx.x;
-    if (tid == 0 && (p.req_offsets[0] != 0 || p.req_offsets[p.n_reqs] != p.n)) pkv::set_error(p.err, KV_DERR_LIST);
+    const int32_t o_first = tid == 0 ? __ldg(p.req_offsets) : 0;  // the offsets' ends, checked below
+    const int32_t o_last = tid == 0 ? __ldg(p.req_offsets + p.n_reqs) : p.n;
     bool nat[kSItems + 1];
     int32_t req[kSItems];
     stage_and_mark<kSItems, kSThreads>(p, 0, sh_src, sh_dst, sh_off, nat, req);
+    if (o_first != 0 || o_last != p.n) pkv::set_error(p.err, KV_DERR_LIST);
     const int32_t i0 = tid * kSItems;
     int32_t my_last = -1;
 #pragma unroll
@@ -427,13 +463,23 @@ __global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __gr
     int32_t unused;
     // natural start open at i0; -1 only when the offsets do not start at 0
     const int32_t s0 = block_exclusive<kSWarps>(my_last, -1, Max(), sh_scan, &unused);
+    // records go to shared memory first: one thread's runs are consecutive records, so direct
+    // stores from a thread's items scatter over a whole warp's range of sectors
+    extern __shared__ __align__(16) kv_xfer_run sh_rec[];  // kSTile records
     const int32_t cnt = resolve_and_write<kSItems, kSWarps>(p, nat, req, i0, 0, p.n, s0, 0, sh_src, sh_dst, sh_scan,
-                                                            KV_DERR_LIST);
+                                                            KV_DERR_LIST, sh_rec);
+    __syncthreads();
+    const int64_t n_out = min((int64_t)cnt, p.capacity);  // records past the capacity are not written
+    const unsigned long long *src64 = reinterpret_cast<const unsigned long long *>(sh_rec);
+    unsigned long long *dst64 = reinterpret_cast<unsigned long long *>(p.runs);
+    for (int64_t w = tid; w < n_out * 3; w += kSThreads) dst64[w] = src64[w];
     if (tid == 0) {
         *p.n_runs = cnt;
         if ((int64_t)cnt > p.capacity) pkv::set_error(p.err, KV_DERR_CAPACITY);
     }
 }
+
+constexpr int kSingleRecordBytes = kSTile * (int)sizeof(kv_xfer_run);
 
 // Launches the single-CTA builder for lists of one tile (the scratch is not touched), else zeroes the look-back scratch (tile counter and tile records: `need` bytes
 // at `scratch`) and launches one CTA per tile.
@@ -453,7 +499,18 @@ int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *sr
     p.n = (int32_t)n_blocks;
     p.cap = max_run_blocks;
     if (n_blocks <= kSTile) {
-        build_xfer_single_kernel<<<1, kSThreads, 0, s>>>(p);
+        static std::mutex mu;
+        static bool configured[64];
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (!configured[dev.device & 63]) {
+                const int st = pkv::cuda_status(cudaFuncSetAttribute(
+                    build_xfer_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleRecordBytes));
+                if (st != KV_OK) return st;
+                configured[dev.device & 63] = true;
+            }
+        }
+        build_xfer_single_kernel<<<1, kSThreads, kSingleRecordBytes, s>>>(p);
         return pkv::cuda_status(cudaGetLastError());
     }
     const int st = pkv::cuda_status(cudaMemsetAsync(scratch, 0, (size_t)need, s));

@@ -58,12 +58,12 @@ def _builder_case(n_reqs, lens, rng, frag=(12, 0.6), n_ids=None):
     return W.csr(W.pop_lists(q, lens))
 
 
-@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4095, 4096, 4097, 6145, 20000, 100003])
+@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096, 5119, 5120, 5121, 6145, 20000, 100003])
 @pytest.mark.parametrize("cap", [0, 1, 2, 7, 32])
 def test_builder_tiles(n, cap):
     """Runs across tile boundaries, long runs, empty requests, all cap variants.
 
-    Lists of up to 4096 entries go to the single-CTA builder (one tile), longer ones to the
+    Lists of up to 5120 entries go to the single-CTA builder (one tile), longer ones to the
     look-back builder (tiles of 2048); the sizes straddle both limits and the look-back tile edges."""
     rng = np.random.default_rng(n * 31 + cap)
     lens = []

@@ -53,7 +53,7 @@ def _host(x: K.XferList):
 
 
 def test_static_builder_matches_workspace_builder_twice():
-    # different lists; those longer than 4096 entries take the look-back builder, which uses the scratch
+    # different lists; those longer than 5120 entries take the look-back builder, which uses the scratch
     cases = [(_lists(1, 9000, 17), 2), (_lists(2, 100000, 3), 0), (_lists(3, 3000, 4), 1), (_lists(4, 70001, 5), 7)]
     dev = [tuple(torch.from_numpy(a).cuda() for a in lists) + (cap,) for lists, cap in cases]
     want = [_host(K.kv_build_xfer_list(o, s, d, cap)) for o, s, d, cap in dev]
