@@ -63,7 +63,7 @@ def test_reduce_max_single_process():
 
 def _reference(env_extra, *args):
     env = dict(os.environ, **env_extra)
-    return subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "mid",
+    return subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
                            "--steps", "2", "--warmup", "1", *args], cwd=ROOT, env=env, capture_output=True,
                           text=True, timeout=600)
 
@@ -76,7 +76,7 @@ def test_reference_arm_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
-    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "mid"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "tiny"
 
 
 def test_reference_arm_other_ranks_print_nothing():
