@@ -1,6 +1,6 @@
 """One pass of the paged KV-cache hot path over one batch, through the C ABI.
 
-A step runs, on one CUDA stream:
+A step runs these calls (3 on a second stream, beside 1 and 2; 4 waits for all three):
   1. kv_slot_mapping        new tokens' slots from the shared block table (when the batch has new tokens)
   2. kv_reshape_and_cache   their K/V rows into every layer's paged tensor
   3. kv_build_xfer_list     the send side's per-request block lists -> contiguous runs
@@ -142,11 +142,24 @@ class TransferStep:
                                self.slice_bytes, self.wl.dst_slice_off, self.req_offsets, self.dst_req_offsets,
                                self.dst_ids, stream=stream)
 
+    def side_stream(self) -> "torch.cuda.Stream":
+        """The second stream the builder runs on (created on first use)."""
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(self.device)
+        return self._side
+
     def run(self, stream=None):
-        self.write_tokens(stream)
-        self.build(stream)
-        self.pack(stream)
-        self.unpack(stream)
+        """The five calls.  The block lists do not depend on the new tokens, so the builder (after
+        the clip, when there is one) runs on a second stream beside slot_mapping and
+        reshape_and_cache; pack waits for both."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        side = self.side_stream()
+        side.wait_stream(main)  # the step's inputs are ready
+        self.build(side)
+        self.write_tokens(main)
+        main.wait_stream(side)
+        self.pack(main)
+        self.unpack(main)
 
     def capture(self, fn=None, stream=None) -> "torch.cuda.CUDAGraph":
         """Capture run() (or another method of this step, e.g. write_tokens) into a CUDA graph for
