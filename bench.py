@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 from paged_kv_cache_81_gb300 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth (context; the roofline uses the measured copy peak)
 PG_TIMEOUT_S = 300  # process-group timeout under torchrun
 KERNEL_NAMES = ("slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack")
 COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_copy.cuh",
@@ -331,7 +332,8 @@ def run_ours(args):
         gbs = per_bytes[name] / (ms * 1e-3) / 1e9
         kernels[name] = {"ms": round(ms, 4), "ms_median": round(statistics.median(per_kernel_all[name]), 4),
                          "ms_best": round(min(per_kernel_all[name]), 4), "bytes": per_bytes[name],
-                         "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+                         "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                         "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
     if step.n_tokens:
         kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
 
@@ -367,6 +369,7 @@ def run_ours(args):
                      "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
                      if peak_kind == "measured" else "of fallback", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": per_bytes[dominant]},
         "kernels": kernels,
         "schedule": "build_xfer_list on a second stream beside slot_mapping + reshape_and_cache; pack, then "
