@@ -252,7 +252,8 @@ def run_ours(args):
             K.kv_reshape_and_cache(step.src, step.new_kv, step.slot)
 
     # the five calls of step.run(), split so that each is bracketed by its own events: the builder
-    # on the step's second stream (beside slot_mapping and reshape_and_cache), the rest on `stream`
+    # on the step's second stream (issued first, beside slot_mapping and reshape_and_cache), the
+    # rest on `stream`
     side = step.side_stream()
 
     def timed_step(e):

@@ -151,7 +151,8 @@ class TransferStep:
     def run(self, stream=None):
         """The five calls.  The block lists do not depend on the new tokens, so the builder (after
         the clip, when there is one) runs on a second stream beside slot_mapping and
-        reshape_and_cache; pack waits for both."""
+        reshape_and_cache; pack waits for both.  The builder is issued first: its one CTA needs a
+        nearly empty SM, which it would not get once reshape_and_cache's grid fills the GPU."""
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         side = self.side_stream()
         side.wait_stream(main)  # the step's inputs are ready
