@@ -143,9 +143,11 @@ class TransferStep:
                                self.dst_ids, stream=stream)
 
     def side_stream(self) -> "torch.cuda.Stream":
-        """The second stream the builder runs on (created on first use)."""
+        """The second stream the builder runs on (created on first use), at the highest priority:
+        its few small CTAs are then placed before reshape_and_cache's as SMs free up."""
         if getattr(self, "_side", None) is None:
-            self._side = torch.cuda.Stream(self.device)
+            lo, hi = torch.cuda.Stream.priority_range()
+            self._side = torch.cuda.Stream(self.device, priority=min(lo, hi))
         return self._side
 
     def run(self, stream=None):
