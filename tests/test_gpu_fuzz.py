@@ -1,0 +1,122 @@
+"""Seeded random geometries through the whole step, bit-exact against the oracle.
+
+Each case draws a cache geometry and a list structure and runs all five calls:
+- geometry: layout pair (separate/separate, latent/latent, or any mix of blocks-first and
+  kv-first), block sizes, heads and head dims, an optional head slice;
+- an optional remap onto another block size and row offset;
+- the run cap;
+- lists: fragmented id queues, empty requests, new tokens at random positions of the
+  requests' blocks.
+The presets cover the configurations of the pages; this covers the combinations between
+them.  Every output is compared: slots, run records, the staging buffer, the source cache
+after the token write and the destination cache after unpack.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_81_gb300 import pagedkv as K
+from paged_kv_cache_81_gb300 import workloads as W
+from tests import gpu_support as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_81_gb300 import build
+    build.build()
+    K.load()
+
+
+MAX_REQS, MAX_BLOCKS_PER_REQ = 5, 12
+
+
+def _geom(layout, bs, row, num_blocks):
+    """A geometry of `row` bytes per token row (a multiple of 16)."""
+    if layout == "mla":
+        return W.CacheGeom("mla", num_blocks, bs, 1, row // 2)
+    return W.CacheGeom(layout, num_blocks, bs, row // 16, 8)
+
+
+def fuzz_workload(seed: int) -> tuple:
+    rng = np.random.default_rng(seed)
+    two_planes = bool(rng.integers(0, 2))
+    if two_planes:
+        src_layout, dst_layout = rng.choice(["blocks_first", "kv_first"], size=2)
+    else:
+        src_layout = dst_layout = str(rng.choice(["separate", "mla"]))
+    bs = int(rng.choice([1, 2, 3, 8, 16]))
+    head_dim = int(rng.choice([8, 16, 24, 64]))
+    heads = 1 if src_layout == "mla" else int(rng.integers(1, 5))
+    row = heads * head_dim * 2
+    slice_off, slice_bytes = 0, 0
+    if heads > 1 and rng.random() < 0.5:
+        h0 = int(rng.integers(0, heads))
+        hn = int(rng.integers(1, heads - h0 + 1))
+        slice_off, slice_bytes = h0 * head_dim * 2, hn * head_dim * 2
+    moved = slice_bytes or row
+    src_blocks = MAX_REQS * MAX_BLOCKS_PER_REQ + int(rng.integers(4, 64))
+    if rng.random() < 0.5:  # whole blocks onto the same geometry (a head slice keeps only that slice)
+        dst_bs, dst_row, dst_off = bs, moved, 0
+    else:  # token-granular remap: another block size, the slice somewhere inside a wider row
+        dst_bs = int(rng.choice([1, 2, 4, 8, 16, 32]))
+        extra = 16 * int(rng.integers(0, 4))
+        dst_row, dst_off = moved + extra, 16 * int(rng.integers(0, extra // 16 + 1))
+    dst_blocks = -(-MAX_REQS * MAX_BLOCKS_PER_REQ * bs // dst_bs) + int(rng.integers(2, 32))
+    wl = W.Workload(f"fuzz{seed}", 100 + seed, "tiny", n_layers=int(rng.integers(1, 4)),
+                    src=_geom(str(src_layout), bs, row, src_blocks),
+                    dst=_geom(str(dst_layout), dst_bs, dst_row, dst_blocks),
+                    slice_off=slice_off, slice_bytes=slice_bytes, dst_slice_off=dst_off)
+    cap = [None, 0, 1, 2, 5][int(rng.integers(0, 5))]
+    return wl, cap, rng
+
+
+def fuzz_case(wl: W.Workload, rng) -> W.Case:
+    bs = wl.src.block_size
+    n = int(rng.integers(1, MAX_REQS + 1))
+    counts = [int(rng.integers(0, MAX_BLOCKS_PER_REQ + 1)) for _ in range(n)]
+    if n > 1 and rng.random() < 0.5:
+        counts[int(rng.integers(0, n))] = 0  # an empty request
+    q = W.fragmented_queue(rng, wl.src.num_blocks, int(rng.integers(1, 9)), float(rng.random()))
+    src_lists = W.pop_lists(q, counts)
+    off, ids = W.csr(src_lists)
+    if wl.equal_geometry:
+        dst_counts = counts
+    else:
+        dst_counts = [W.blocks_for(c * bs, wl.dst.block_size) for c in counts]
+    qd = W.fragmented_queue(rng, wl.dst.num_blocks, int(rng.integers(1, 9)), float(rng.random()))
+    doff, dids = W.csr(W.pop_lists(qd, dst_counts))
+    width = max(1, max(counts))
+    table = np.full((n, width), -1, dtype=np.int32)
+    for r, l in enumerate(src_lists):
+        table[r, :len(l)] = l
+    token_req, token_pos = [], []
+    for r, c in enumerate(counts):
+        if c == 0:
+            continue
+        k = int(rng.integers(0, min(6, c * bs) + 1))
+        pos = rng.choice(c * bs, size=k, replace=False)
+        token_req += [r] * k
+        token_pos += [int(p) for p in pos]
+    tr = np.asarray(token_req, dtype=np.int32) if token_req else None
+    tp = np.asarray(token_pos, dtype=np.int32) if token_pos else None
+    return W.Case(wl, off, ids, doff, dids, table if tr is not None else None, tr, tp,
+                  req_tokens=np.asarray([c * bs for c in counts], dtype=np.int32))
+
+
+@pytest.mark.parametrize("seed", range(160))
+def test_fuzz_step_matches_oracle(seed):
+    wl, cap, rng = fuzz_workload(seed)
+    case = fuzz_case(wl, rng)
+    src, dst, new = G.host_inputs(wl, case, seed=seed + 5000)
+    gpu = G.run_gpu(wl, case, src, dst, new, max_run_blocks=cap)
+    ora = G.run_oracle(wl, case, src, dst, new, gpu["max_run_blocks"])
+    what = (f"seed {seed}: {wl.src.layout}->{wl.dst.layout} bs {wl.src.block_size}->{wl.dst.block_size} "
+            f"row {wl.src.row_bytes}->{wl.dst.row_bytes} slice {wl.slice_off}+{wl.moved_slice}@{wl.dst_slice_off} "
+            f"layers {wl.n_layers} cap {cap} blocks {case.n_blocks} tokens {case.n_tokens}")
+    G.compare(gpu, ora, what)
