@@ -30,12 +30,13 @@ def _new_shape(g: W.CacheGeom, T: int):
     return (T, 1, g.heads * g.head_dim) if g.layout == "mla" else (T, g.heads, g.head_dim)
 
 
-def run_gpu(wl, case, src, dst, new, max_run_blocks=None, device="cuda"):
+def run_gpu(wl, case, src, dst, new, max_run_blocks=None, device="cuda", host_stage=False):
     s_dev = W.to_device_bf16(src, device)
     d_dev = W.to_device_bf16(dst, device) if dst is not None else None
     n_dev = [x.reshape(_new_shape(wl.src, case.n_tokens)) for x in W.to_device_bf16(new, device)]
     K.kv_get_last_error(clear=True)
-    step = TransferStep(wl, case, s_dev, d_dev, n_dev, max_run_blocks=max_run_blocks, device=device)
+    step = TransferStep(wl, case, s_dev, d_dev, n_dev, max_run_blocks=max_run_blocks, device=device,
+                        host_stage=host_stage)
     step.run()
     torch.cuda.synchronize()
     out = dict(

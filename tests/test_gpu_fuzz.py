@@ -4,7 +4,7 @@ Each case draws a cache geometry and a list structure and runs all five calls:
 - geometry: layout pair (separate/separate, latent/latent, or any mix of blocks-first and
   kv-first), block sizes, heads and head dims, an optional head slice;
 - an optional remap onto another block size and row offset;
-- the run cap;
+- the run cap, and staging in HBM or in pinned host memory;
 - lists: fragmented id queues, empty requests, new tokens at random positions of the
   requests' blocks.
 The presets cover the configurations of the pages; this covers the combinations between
@@ -76,6 +76,11 @@ def fuzz_workload(seed: int) -> tuple:
     return wl, cap, rng
 
 
+def fuzz_host_stage(seed: int) -> bool:
+    """A quarter of the cases stage in pinned host memory (the spill target) instead of HBM."""
+    return seed % 4 == 3
+
+
 def fuzz_case(wl: W.Workload, rng) -> W.Case:
     bs = wl.src.block_size
     n = int(rng.integers(1, MAX_REQS + 1))
@@ -114,9 +119,10 @@ def test_fuzz_step_matches_oracle(seed):
     wl, cap, rng = fuzz_workload(seed)
     case = fuzz_case(wl, rng)
     src, dst, new = G.host_inputs(wl, case, seed=seed + 5000)
-    gpu = G.run_gpu(wl, case, src, dst, new, max_run_blocks=cap)
+    host_stage = fuzz_host_stage(seed)
+    gpu = G.run_gpu(wl, case, src, dst, new, max_run_blocks=cap, host_stage=host_stage)
     ora = G.run_oracle(wl, case, src, dst, new, gpu["max_run_blocks"])
     what = (f"seed {seed}: {wl.src.layout}->{wl.dst.layout} bs {wl.src.block_size}->{wl.dst.block_size} "
             f"row {wl.src.row_bytes}->{wl.dst.row_bytes} slice {wl.slice_off}+{wl.moved_slice}@{wl.dst_slice_off} "
-            f"layers {wl.n_layers} cap {cap} blocks {case.n_blocks} tokens {case.n_tokens}")
+            f"layers {wl.n_layers} cap {cap} blocks {case.n_blocks} tokens {case.n_tokens} host stage {host_stage}")
     G.compare(gpu, ora, what)
