@@ -16,6 +16,10 @@
 //   prefix at b:          last natural start before b and the number of run starts before b.
 // The cap's starts in a stretch [a, b) with no natural start, continuing a run opened at
 // s < a, are counted in closed form: floor((b-1-s)/cap) - floor((a-1-s)/cap).
+//
+// A list of at most one single-CTA tile (5120 entries) takes a second kernel instead: one
+// CTA of 1024 threads, no look-back and no scratch, its run records staged in shared memory
+// and written out contiguously.
 #include <algorithm>
 #include <mutex>
 
@@ -432,6 +436,7 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
 // without the look-back, so it needs neither the scratch nor its zeroing.  A short list
 // (a decode-side request, a few prompts) is then one launch.  Longer lists go to the
 // look-back kernel: one CTA walking several tiles in turn is slower than one CTA per tile.
+// The run records go through kSTile * 24 bytes of dynamic shared memory (see below).
 // ---------------------------------------------------------------------------
 #ifndef PKV_XFER_SINGLE_ITEMS
 #define PKV_XFER_SINGLE_ITEMS 5
