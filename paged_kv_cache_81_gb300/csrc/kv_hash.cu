@@ -122,6 +122,9 @@ __device__ __forceinline__ bool request_blocks(const int32_t *off, int32_t r, in
 
 // ---- without a workspace: one thread walks each request's bytes ----
 constexpr int kChainThreads = 128;
+#ifndef PKV_HASH_CHAIN_GROUP
+#define PKV_HASH_CHAIN_GROUP 16  // token loads in flight ahead of the chain (1, 4, 16 measured; 16 best)
+#endif
 
 __global__ void __launch_bounds__(kChainThreads) hash_chain_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
                                                                    const int32_t *__restrict__ tokens,
@@ -140,12 +143,13 @@ __global__ void __launch_bounds__(kChainThreads) hash_chain_kernel(const int32_t
             Fnv h = fnv_block_start(parent);
             const int32_t *tb = t + (int64_t)b * bs;
             int32_t j = 0;
-            for (; j + 4 <= bs; j += 4) {  // four loads issued before their bytes enter the chain
-                uint32_t v[4];
+            // token loads issued a group at a time, ahead of the bytes entering the chain
+            for (; j + PKV_HASH_CHAIN_GROUP <= bs; j += PKV_HASH_CHAIN_GROUP) {
+                uint32_t v[PKV_HASH_CHAIN_GROUP];
 #pragma unroll
-                for (int q = 0; q < 4; q++) v[q] = (uint32_t)__ldg(tb + j + q);
+                for (int q = 0; q < PKV_HASH_CHAIN_GROUP; q++) v[q] = (uint32_t)__ldg(tb + j + q);
 #pragma unroll
-                for (int q = 0; q < 4; q++) h = fnv_bytes<4>(h, v[q]);
+                for (int q = 0; q < PKV_HASH_CHAIN_GROUP; q++) h = fnv_bytes<4>(h, v[q]);
             }
             for (; j < bs; j++) h = fnv_bytes<4>(h, (uint32_t)__ldg(tb + j));
             parent = fnv_value(h);
