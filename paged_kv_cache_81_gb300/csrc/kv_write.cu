@@ -78,6 +78,10 @@ struct ReshapeParams {
 #define PKV_RESHAPE_PLANE_MAJOR 0  // 1: order work (plane, token, chunk) instead of (token, plane, chunk)
 #endif
 constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
+#ifndef PKV_WRITE_SPLIT_ITERATIONS
+#define PKV_WRITE_SPLIT_ITERATIONS 2  // kv_write_tokens: grid-stride iterations per thread above which it splits
+#endif
+constexpr int64_t kWriteSplitIterations = PKV_WRITE_SPLIT_ITERATIONS;
 
 // The slot of token `tok`: the block table's entry for the token's logical block times the
 // block size plus the offset in the block, or -1 for an invalid token.
@@ -159,15 +163,19 @@ __global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
     }
 }
 
-// Validation and launches shared by kv_reshape_and_cache and kv_write_tokens.
-template <bool FUSED>
-int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride, int64_t n_tokens,
-                ReshapeParams p, cudaStream_t stream)
+// Argument checks of a row write (kv_reshape_and_cache, kv_write_tokens).  KV_OK with
+// *nothing = true when there is nothing to launch.
+int validate_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride, int64_t n_tokens,
+                  bool *nothing)
 {
+    *nothing = false;
     int st = pkv::check_cache(cache);
     if (st != KV_OK) return st;
     if (n_tokens < 0 || new_token_stride < 0) return KV_ERR_INVALID_ARG;
-    if (n_tokens == 0 || cache->n_tensors == 0) return KV_OK;
+    if (n_tokens == 0 || cache->n_tensors == 0) {
+        *nothing = true;
+        return KV_OK;
+    }
     if (new_kv == nullptr) return KV_ERR_INVALID_ARG;
     if (!pkv::aligned16(new_token_stride)) return KV_ERR_ALIGN;
     if (new_token_stride < cache->row_bytes) return KV_ERR_RANGE;
@@ -179,6 +187,32 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
     const int64_t cpr = cache->row_bytes / 16;
     const int64_t total = n_tokens * cache->n_planes * cpr;
     if (slot_limit >= (1ll << 31) || total >= (1ll << 31) || cpr >= (1ll << 31)) return KV_ERR_UNSUPPORTED;
+    return KV_OK;
+}
+
+constexpr int kRowThreads = 256;
+
+// CTAs per tensor of a row-write launch: enough for the work, at most about four waves of
+// 8 resident CTAs per SM over the nt tensors of the launch.
+void row_grid(const kv_cache_desc *cache, int64_t n_tokens, int32_t nt, const pkv::DeviceInfo &dev, int64_t *need,
+              int64_t *cap)
+{
+    const int64_t total = n_tokens * cache->n_planes * (cache->row_bytes / 16);
+    *need = (total + (int64_t)kRowThreads * kReshapeUnroll - 1) / ((int64_t)kRowThreads * kReshapeUnroll);
+    *cap = std::max<int64_t>(1, ((int64_t)dev.num_sms * 8 * 4 + nt - 1) / nt);
+}
+
+// Launches shared by kv_reshape_and_cache and kv_write_tokens (arguments already validated).
+template <bool FUSED>
+int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride, int64_t n_tokens,
+                ReshapeParams p, cudaStream_t stream)
+{
+    bool nothing = false;
+    int st = validate_rows(cache, new_kv, new_token_stride, n_tokens, &nothing);
+    if (st != KV_OK || nothing) return st;
+    const int64_t slot_limit = cache->num_blocks * (int64_t)cache->block_size;
+    const int64_t cpr = cache->row_bytes / 16;
+    const int64_t total = n_tokens * cache->n_planes * cpr;
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
 
@@ -195,8 +229,6 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
     p.n_planes = cache->n_planes;
     p.err = dev->err_word;
 
-    const int threads = 256;
-    const int64_t per_tensor_ctas = (total + (int64_t)threads * kReshapeUnroll - 1) / ((int64_t)threads * kReshapeUnroll);
     int64_t *slot_out = p.slot_out;
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
         const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
@@ -206,10 +238,10 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
                 p.src[t * cache->n_planes + pl] = new_kv[(int64_t)(t0 + t) * cache->n_planes + pl];
         }
         p.slot_out = t0 == 0 ? slot_out : nullptr;
-        // about four waves of 8 resident CTAs per SM over all tensors of the launch
-        const int64_t cap = std::max<int64_t>(1, ((int64_t)dev->num_sms * 8 * 4 + nt - 1) / nt);
+        int64_t per_tensor_ctas, cap;
+        row_grid(cache, n_tokens, nt, *dev, &per_tensor_ctas, &cap);
         const dim3 grid((unsigned)std::min(per_tensor_ctas, cap), (unsigned)nt);
-        reshape_and_cache_kernel<FUSED><<<grid, threads, 0, stream>>>(p);
+        reshape_and_cache_kernel<FUSED><<<grid, kRowThreads, 0, stream>>>(p);
         st = pkv::cuda_status(cudaGetLastError());
         if (st != KV_OK) return st;
     }
@@ -261,6 +293,25 @@ int kv_write_tokens(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t 
                          (n_reqs > 0 && max_blocks_per_req > 0 && block_table == nullptr)))
         return KV_ERR_INVALID_ARG;
     if (n_reqs > 0 && bt_row_stride < max_blocks_per_req) return KV_ERR_INVALID_ARG;
+    // A large batch walks several grid-stride iterations per thread, and in the fused kernel
+    // each waits on the table lookup's dependent loads.  With slot_out given, such a batch
+    // runs as slot_mapping into slot_out followed by the plain row copy: the same results,
+    // one extra launch.
+    bool nothing = false;
+    int st = validate_rows(cache, new_kv, new_token_stride, n_tokens, &nothing);
+    if (st != KV_OK || nothing) return st;
+    if (slot_out != nullptr) {
+        const pkv::DeviceInfo *dev = pkv::current_device();
+        if (dev == nullptr) return KV_ERR_CUDA;
+        int64_t need, cap;
+        row_grid(cache, n_tokens, std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors), *dev, &need, &cap);
+        if (need > kWriteSplitIterations * cap) {
+            st = kv_slot_mapping(block_table, n_reqs, max_blocks_per_req, bt_row_stride, token_req, token_pos,
+                                 n_tokens, cache->block_size, slot_out, stream);
+            if (st != KV_OK) return st;
+            return kv_reshape_and_cache(cache, new_kv, new_token_stride, slot_out, n_tokens, stream);
+        }
+    }
     ReshapeParams p{};
     p.table = block_table;
     p.token_req = token_req;

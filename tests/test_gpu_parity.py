@@ -404,6 +404,39 @@ def test_write_tokens_fused_matches_oracle(wl):
         np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
 
 
+@pytest.mark.parametrize("with_slot_out", [True, False], ids=["split", "fused"])
+def test_write_tokens_large_batch(with_slot_out):
+    """A prefill large enough that kv_write_tokens runs slot_mapping and the row copy as two
+    launches when it may write slot_out; without slot_out the same batch stays fused."""
+    g = W.CacheGeom("blocks_first", 1024, 16, 1, 128)
+    wl = W.Workload("write_large", 90, "page", n_layers=48, src=g, dst=g)
+    rng = np.random.default_rng(91)
+    ids = rng.choice(g.num_blocks, size=4 * 128, replace=False).astype(np.int32)
+    table = ids.reshape(4, 128)
+    token_req = np.repeat(np.arange(4, dtype=np.int32), 2048)
+    token_pos = np.tile(np.arange(2048, dtype=np.int32), 4)
+    src = W.host_cache_tensors(g, wl.n_tensors, rng)
+    new = [W.normal_bf16_bytes(rng, 8192 * g.row_bytes // 2).reshape(8192, g.row_bytes // 2)
+           for _ in range(wl.n_tensors * g.n_planes)]
+    s_dev = W.to_device_bf16(src, "cuda")
+    n_dev = [x.reshape(8192, g.heads, g.head_dim) for x in W.to_device_bf16(new, "cuda")]
+    cache = K.PagedCache.from_tensors(s_dev, g.layout)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    slot = torch.full((8192,), -7, dtype=torch.int64, device="cuda") if with_slot_out else None
+    K.kv_get_last_error(clear=True)
+    K.kv_write_tokens(cache, n_dev, t(table), t(token_req), t(token_pos), slot)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error() == 0
+    want_slot, bad = oracle.slot_mapping(table, token_req, token_pos, g.block_size)
+    assert bad == 0
+    if with_slot_out:
+        np.testing.assert_array_equal(slot.cpu().numpy(), want_slot)
+    sc = H.ora_cache(g, [a.copy() for a in src])
+    assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], want_slot) == 0
+    for a, b in zip(s_dev, sc.tensors):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+
+
 def test_write_tokens_invalid_tokens():
     g = W.CacheGeom("separate", 8, 4, 1, 64)
     host = W.host_cache_tensors(g, 1, np.random.default_rng(2))
