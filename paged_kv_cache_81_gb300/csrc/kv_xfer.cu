@@ -376,50 +376,74 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
     block_exclusive(known, 0, Sum(), sh_scan, &tile_cnt);
 
     // ---- publish, look back, publish the inclusive prefix ----
-    if (tid == 0) {
+    // Warp 0 looks back 32 predecessor tiles at a time: lane l reads tile j - l.  The nearest
+    // lane holding an inclusive prefix (a tile before the list counts, with prefix {-1, 0})
+    // bounds the window; every tile between it and this one must have published its
+    // aggregate, else the window is read again (bounded wait).  The aggregates are then
+    // folded nearest first, and the prefix applied.  Every lane computes the same values.
+    if (tid < 32) {
+        const int lane = tid;
         const Agg agg{tile_first == 0x7fffffff ? -1 : tile_first, tile_last, tile_cnt};
         TileRecord *rec = p.tiles + tile;
         Pre excl{-1, 0};
         if (tile > 0) {
-            rec->first_nat = agg.first_nat;
-            rec->last_nat = agg.last_nat;
-            rec->cnt = agg.cnt;
-            st_release(&rec->flag, 1);
+            if (lane == 0) {
+                rec->first_nat = agg.first_nat;
+                rec->last_nat = agg.last_nat;
+                rec->cnt = agg.cnt;
+                st_release(&rec->flag, 1);
+            }
             Agg suffix{-1, -1, 0};  // aggregate of [(j + 1) * kTile, tile_start)
-            int32_t j = tile - 1;
+            int32_t j = tile - 1;    // nearest tile not yet folded in
             const unsigned long long t_begin = global_ns();
             unsigned ns = 32;
             while (true) {
-                const TileRecord *pr = p.tiles + j;
-                int32_t f = ld_acquire(&pr->flag);
-                if (f == 0) {
-                    if (global_ns() - t_begin > kWaitLimitNs) {
-                        pkv::set_error(p.err, KV_DERR_TIMEOUT);
+                const int32_t jj = j - lane;
+                int32_t f = 2;
+                Pre pj{-1, 0};
+                Agg aj{-1, -1, 0};
+                if (jj >= 0) {
+                    const TileRecord *pr = p.tiles + jj;
+                    f = ld_acquire(&pr->flag);
+                    if (f == 2) pj = Pre{__ldcg(&pr->pre_s), __ldcg(&pr->pre_cnt)};
+                    else if (f == 1) aj = Agg{__ldcg(&pr->first_nat), __ldcg(&pr->last_nat), __ldcg(&pr->cnt)};
+                }
+                const unsigned pre_mask = __ballot_sync(0xffffffffu, f == 2);
+                const int p_lane = pre_mask ? __ffs(pre_mask) - 1 : 32;
+                const unsigned before = p_lane >= 32 ? 0xffffffffu : (1u << p_lane) - 1u;
+                if (__ballot_sync(0xffffffffu, f == 0) & before) {
+                    const int expired = __shfl_sync(0xffffffffu, lane == 0 ? (int)(global_ns() - t_begin > kWaitLimitNs) : 0, 0);
+                    if (expired) {
+                        if (lane == 0) pkv::set_error(p.err, KV_DERR_TIMEOUT);
                         break;  // give up: prefix left at {-1, 0}
                     }
                     __nanosleep(ns);
                     ns = min(ns * 2u, 1024u);
                     continue;
                 }
-                const int32_t m = (j + 1) * kTile;
-                if (f == 2) {
-                    const Pre pj{__ldcg(&pr->pre_s), __ldcg(&pr->pre_cnt)};
-                    excl = apply(suffix, m, tile_start, pj, p.cap);
+                for (int k = 0; k < p_lane; k++) {  // tiles j, j - 1, ..., j - p_lane + 1
+                    const Agg ak{__shfl_sync(0xffffffffu, aj.first_nat, k), __shfl_sync(0xffffffffu, aj.last_nat, k),
+                                 __shfl_sync(0xffffffffu, aj.cnt, k)};
+                    suffix = combine(ak, suffix, (j - k + 1) * kTile, tile_start, p.cap);
+                }
+                if (p_lane < 32) {
+                    const Pre pp{__shfl_sync(0xffffffffu, pj.s, p_lane), __shfl_sync(0xffffffffu, pj.cnt, p_lane)};
+                    excl = apply(suffix, (j - p_lane + 1) * kTile, tile_start, pp, p.cap);
                     break;
                 }
-                const Agg aj{__ldcg(&pr->first_nat), __ldcg(&pr->last_nat), __ldcg(&pr->cnt)};
-                suffix = combine(aj, suffix, m, tile_start, p.cap);
-                j--;
+                j -= 32;
             }
         }
-        const Pre incl = apply(agg, tile_start, tile_end, excl, p.cap);
-        rec->pre_s = incl.s;
-        rec->pre_cnt = incl.cnt;
-        st_release(&rec->flag, 2);
-        sh_pre = excl;
-        if (tile_end == p.n) {
-            *p.n_runs = incl.cnt;
-            if ((int64_t)incl.cnt > p.capacity) pkv::set_error(p.err, KV_DERR_CAPACITY);
+        if (lane == 0) {
+            const Pre incl = apply(agg, tile_start, tile_end, excl, p.cap);
+            rec->pre_s = incl.s;
+            rec->pre_cnt = incl.cnt;
+            st_release(&rec->flag, 2);
+            sh_pre = excl;
+            if (tile_end == p.n) {
+                *p.n_runs = incl.cnt;
+                if ((int64_t)incl.cnt > p.capacity) pkv::set_error(p.err, KV_DERR_CAPACITY);
+            }
         }
     }
     __syncthreads();
