@@ -60,6 +60,8 @@ def parse():
                     help="clip every request's block lists to the last N tokens before the xfer_list (0 = off)")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling captures)")
     ap.add_argument("--num-blocks", type=int, default=None, help="override blocks per tensor (profiling captures)")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="host->device streams the e2e leg splits each step's new rows over")
     ap.add_argument("--hash-only", action="store_true",
                     help="run only the prefix-hash measurement (kv_block_hashes), e.g. to profile its kernels")
     return ap.parse_args()
@@ -586,6 +588,9 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
 
     comp = stream
     copy_stream = torch.cuda.Stream(dev)
+    n_split = max(1, int(getattr(args, "e2e_copy_streams", 1)))
+    row_streams = [copy_stream] + [torch.cuda.Stream(dev) for _ in range(n_split - 1)]
+    row_done = [[torch.cuda.Event() for _ in row_streams] for _ in range(2)]
     names = ["req_offsets", "src_ids", "dst_req_offsets", "dst_ids"]
     if step.n_tokens:
         names += ["block_table", "token_req", "token_pos"]
@@ -623,8 +628,18 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
         with torch.cuda.stream(copy_stream):
             for n in names:
                 sets[b][n].copy_(host[n], non_blocking=True)
-            if host_rows is not None:
-                sets[b]["_rows"].copy_(host_rows, non_blocking=True)
+        if host_rows is not None:
+            # the new rows, split over the copy streams (equal byte ranges of the one buffer)
+            src_flat, dst_flat = host_rows.view(-1), sets[b]["_rows"].view(-1)
+            edges = [src_flat.numel() * i // len(row_streams) for i in range(len(row_streams) + 1)]
+            for i, rs in enumerate(row_streams):
+                if rs is not copy_stream:
+                    rs.wait_stream(copy_stream)
+                with torch.cuda.stream(rs):
+                    dst_flat[edges[i]:edges[i + 1]].copy_(src_flat[edges[i]:edges[i + 1]], non_blocking=True)
+                if rs is not copy_stream:
+                    row_done[b][i].record(rs)
+                    copy_stream.wait_event(row_done[b][i])
         if timing["on"]:
             c_end[k].record(copy_stream)
         copied[b].record(copy_stream)
@@ -671,7 +686,8 @@ def run_e2e(args, wl, case, step, dev, stream, K, world, barrier):
     value = world * step.bytes().total * steps / secs / 1e9
     out = {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": steps, "ms_per_step": round(secs / steps * 1e3, 4),
-           "pipelined": "input copies of step k+1 (second stream, double-buffered) overlap step k"}
+           "pipelined": "input copies of step k+1 (second stream, double-buffered) overlap step k",
+           "copy_streams": len(row_streams)}
     if host_rows is not None:
         # this machine's host->device link, measured on the same pinned buffer: the bound of the leg
         link = measure_host_link(host_rows.view(torch.uint8).reshape(-1), dev, comp, reps=3)["h2d_gbs"]
