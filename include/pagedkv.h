@@ -323,7 +323,9 @@ KV_API int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const
  * max_run_blocks, stage_buf: as for kv_pack_blocks (pinned host staging is read over the
  * host link).
  * stage->n_tensors and n_planes must equal dst's.  Destination ids must be distinct:
- * two staged rows aimed at one destination row race.
+ * two staged rows aimed at one destination row race.  A call with nothing staged
+ * (stage->n_blocks == 0) returns KV_OK before the mode is looked at, so an empty
+ * destination list passed as a null dst_ids is fine.
  */
 KV_API int kv_unpack_blocks(const kv_cache_desc *dst, int32_t dst_slice_off, const kv_stage_desc *stage,
                      const kv_xfer_run *runs, const int32_t *n_runs, int64_t run_capacity,

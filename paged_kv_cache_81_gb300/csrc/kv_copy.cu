@@ -385,12 +385,14 @@ int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_off, con
         return KV_ERR_INVALID_ARG;
     if (dst_slice_off < 0 || dst_slice_off + (int64_t)stage->slice_bytes > dst->row_bytes) return KV_ERR_RANGE;
     if (!pkv::aligned16((int64_t)dst_slice_off)) return KV_ERR_ALIGN;
+    // Nothing staged: nothing to copy in either mode.  (An empty destination list may then
+    // arrive as a null dst_ids, which would otherwise read as whole-block mode.)
+    if (dst->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0)
+        return signal != nullptr ? pkv::post_signal(signal, add, (cudaStream_t)stream) : KV_OK;
     const bool remap = dst_ids != nullptr;
     if (remap && (src_req_offsets == nullptr || dst_req_offsets == nullptr || n_reqs < 0))
         return KV_ERR_INVALID_ARG;
     if (!remap && stage->block_size != dst->block_size) return KV_ERR_INVALID_ARG;
-    if (dst->n_tensors == 0 || stage->n_blocks == 0 || run_capacity == 0)
-        return signal != nullptr ? pkv::post_signal(signal, add, (cudaStream_t)stream) : KV_OK;
     if (runs == nullptr || n_runs == nullptr) return KV_ERR_INVALID_ARG;
     int mode = REMAP;
     if (!remap) mode = cache_mode(dst, dst_slice_off, stage->slice_bytes);

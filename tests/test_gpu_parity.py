@@ -292,6 +292,22 @@ def test_host_argument_errors():
     assert K.kv_get_last_error() == 0
 
 
+def test_empty_remap_step():
+    """A remap step (another block size on the receiver) whose requests are all empty: every call
+    succeeds and nothing is written, although the empty destination list reaches the library as a
+    null pointer."""
+    src_g, dst_g = W.CacheGeom("separate", 16, 4, 1, 64), W.CacheGeom("separate", 8, 8, 1, 64)
+    wl = W.Workload("empty_remap", 95, "tiny", n_layers=1, src=src_g, dst=dst_g)
+    assert not wl.equal_geometry
+    z = np.zeros(3, dtype=np.int32)
+    case = W.Case(wl, z, np.zeros(0, np.int32), z.copy(), np.zeros(0, np.int32),
+                  req_tokens=np.zeros(2, np.int32))
+    src, dst, new = G.host_inputs(wl, case, seed=96)
+    gpu = G.run_gpu(wl, case, src, dst, new)
+    ora = G.run_oracle(wl, case, src, dst, new, gpu["max_run_blocks"])
+    G.compare(gpu, ora, "empty remap step")
+
+
 @pytest.mark.parametrize("layout", ["separate", "blocks_first"])
 def test_more_tensors_than_one_launch_carries(layout):
     """130 and 257 cache tensors: reshape_and_cache, pack and unpack split into several launches
