@@ -5,8 +5,9 @@ Each case draws a cache geometry and a list structure and runs all five calls:
   kv-first), block sizes, heads and head dims, an optional head slice;
 - an optional remap onto another block size and row offset;
 - the run cap, and staging in HBM or in pinned host memory;
-- lists: fragmented id queues, empty requests, new tokens at random positions of the
-  requests' blocks.
+- lists: fragmented id queues, empty requests, requests sharing a prefix of block ids (prefix
+  caching: the shared blocks are read more than once), new tokens at random positions of each
+  request's own blocks.
 The presets cover the configurations of the pages; this covers the combinations between
 them.  Every output is compared: slots, run records, the staging buffer, the source cache
 after the token write and the destination cache after unpack.
@@ -33,7 +34,7 @@ def _lib():
     K.load()
 
 
-MAX_REQS, MAX_BLOCKS_PER_REQ = 5, 12
+MAX_REQS, MAX_BLOCKS_PER_REQ = 5, 24
 
 
 def _geom(layout, bs, row, num_blocks):
@@ -72,7 +73,7 @@ def fuzz_workload(seed: int) -> tuple:
                     src=_geom(str(src_layout), bs, row, src_blocks),
                     dst=_geom(str(dst_layout), dst_bs, dst_row, dst_blocks),
                     slice_off=slice_off, slice_bytes=slice_bytes, dst_slice_off=dst_off)
-    cap = [None, 0, 1, 2, 5][int(rng.integers(0, 5))]
+    cap = [None, 0, 1, 2, 5, 16][int(rng.integers(0, 6))]
     return wl, cap, rng
 
 
@@ -88,7 +89,15 @@ def fuzz_case(wl: W.Workload, rng) -> W.Case:
     if n > 1 and rng.random() < 0.5:
         counts[int(rng.integers(0, n))] = 0  # an empty request
     q = W.fragmented_queue(rng, wl.src.num_blocks, int(rng.integers(1, 9)), float(rng.random()))
-    src_lists = W.pop_lists(q, counts)
+    src_lists = [list(l) for l in W.pop_lists(q, counts)]
+    # prefix caching: some requests start with request 0's first blocks (shared source ids)
+    shared = [0] * n
+    if n > 1 and counts[0] > 0 and rng.random() < 0.3:
+        for r in range(1, n):
+            if counts[r] > 0 and rng.random() < 0.5:
+                k = int(rng.integers(1, min(counts[0], counts[r]) + 1))
+                src_lists[r][:k] = src_lists[0][:k]
+                shared[r] = k
     off, ids = W.csr(src_lists)
     if wl.equal_geometry:
         dst_counts = counts
@@ -102,10 +111,11 @@ def fuzz_case(wl: W.Workload, rng) -> W.Case:
         table[r, :len(l)] = l
     token_req, token_pos = [], []
     for r, c in enumerate(counts):
-        if c == 0:
+        own = (c - shared[r]) * bs  # new tokens only in the request's own blocks: slots stay distinct
+        if own <= 0:
             continue
-        k = int(rng.integers(0, min(6, c * bs) + 1))
-        pos = rng.choice(c * bs, size=k, replace=False)
+        k = int(rng.integers(0, min(6, own) + 1))
+        pos = shared[r] * bs + rng.choice(own, size=k, replace=False)
         token_req += [r] * k
         token_pos += [int(p) for p in pos]
     tr = np.asarray(token_req, dtype=np.int32) if token_req else None
@@ -114,7 +124,7 @@ def fuzz_case(wl: W.Workload, rng) -> W.Case:
                   req_tokens=np.asarray([c * bs for c in counts], dtype=np.int32))
 
 
-@pytest.mark.parametrize("seed", range(160))
+@pytest.mark.parametrize("seed", range(400))
 def test_fuzz_step_matches_oracle(seed):
     wl, cap, rng = fuzz_workload(seed)
     case = fuzz_case(wl, rng)
