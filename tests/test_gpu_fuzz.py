@@ -9,7 +9,8 @@ Each case draws a cache geometry and a list structure and runs all five calls:
   caching: the shared blocks are read more than once), new tokens at random positions of each
   request's own blocks.
 The presets cover the configurations of the pages; this covers the combinations between
-them.  Every output is compared: slots, run records, the staging buffer, the source cache
+them.  Two more fuzzes drive the builder alone (lists up to 120K entries) and the prefix hash
+(block sizes 1 to 700) against the oracle.  Every output is compared: slots, run records, the staging buffer, the source cache
 after the token write and the destination cache after unpack.
 """
 from __future__ import annotations
@@ -18,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_81_gb300 import pagedkv as K
 from paged_kv_cache_81_gb300 import workloads as W
 from tests import gpu_support as G
@@ -136,3 +138,51 @@ def test_fuzz_step_matches_oracle(seed):
             f"row {wl.src.row_bytes}->{wl.dst.row_bytes} slice {wl.slice_off}+{wl.moved_slice}@{wl.dst_slice_off} "
             f"layers {wl.n_layers} cap {cap} blocks {case.n_blocks} tokens {case.n_tokens} host stage {host_stage}")
     G.compare(gpu, ora, what)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_builder_matches_oracle(seed):
+    """Random lists from 1 to 120K entries, across the single-CTA / look-back boundary and many
+    look-back tiles: request count and lengths, id contiguity, destination ids, the cap, and the
+    workspace or static entry point."""
+    rng = np.random.default_rng(10_000 + seed)
+    n = int(rng.choice([int(rng.integers(1, 6000)), int(rng.integers(5000, 12000)), int(rng.integers(1, 120_000))]))
+    lens, left = [], n
+    while left > 0:
+        k = int(min(left, rng.integers(0, max(2, n // int(rng.integers(1, 64)) + 2))))
+        lens.append(k)
+        left -= k
+    q = W.fragmented_queue(rng, n + int(rng.integers(0, 50)), int(rng.integers(1, 40)), float(rng.random()))
+    off, ids = W.csr(W.pop_lists(q, lens))
+    dids = W.fragmented_queue(rng, n + 9, int(rng.integers(1, 40)), float(rng.random()))[:n].astype(np.int32)
+    cap = int(rng.choice([0, 1, 2, 3, 7, 32, 1000]))
+    with_dst = bool(rng.integers(0, 2))
+    builder = K.kv_build_xfer_list_static if rng.integers(0, 2) else K.kv_build_xfer_list
+    x = builder(torch.from_numpy(off).cuda(), torch.from_numpy(ids).cuda(),
+                torch.from_numpy(dids).cuda() if with_dst else None, cap)
+    torch.cuda.synchronize()
+    got = x.host()
+    want = oracle.build_xfer_list(off, ids, dids if with_dst else None, cap)
+    assert got["count"] == want["req"].shape[0]
+    for key in want:
+        np.testing.assert_array_equal(got[key], want[key], err_msg=f"{key}: n {n} cap {cap} dst {with_dst}")
+    assert K.kv_get_last_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_hashes_match_oracle(seed):
+    """Random token batches: block sizes 1 to 700, up to 39 requests of any length, any token
+    values and seed; both device paths."""
+    rng = np.random.default_rng(20_000 + seed)
+    bs = int(rng.choice([1, 2, 3, 5, 16, 17, 64, 80, 512, 700]))
+    lens = rng.integers(0, bs * int(rng.integers(1, 40)) + 1, size=int(rng.integers(1, 40)))
+    toks = [rng.integers(-2 ** 31, 2 ** 31, size=int(l), dtype=np.int64).astype(np.int32) for l in lens]
+    off, flat = W.csr(toks)
+    hseed = int(rng.integers(0, 2 ** 63))
+    want_o, want = oracle.block_hashes(off, flat, bs, hseed)
+    for ws in ("auto", None):
+        o, h = K.kv_block_hashes(torch.from_numpy(off).cuda(), torch.from_numpy(flat).cuda(), bs, hseed, workspace=ws)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(o.cpu().numpy(), want_o)
+        np.testing.assert_array_equal(h[:int(want_o[-1])].cpu().numpy().view(np.uint64), want, err_msg=f"ws {ws}")
+    assert K.kv_get_last_error() == 0
