@@ -292,6 +292,35 @@ def test_host_argument_errors():
     assert K.kv_get_last_error() == 0
 
 
+@pytest.mark.parametrize("heads", [4, 8], ids=["8KiB_blocks_warp_engine", "16KiB_blocks_tma_engine"])
+def test_run_past_the_staging_buffer_flagged(heads):
+    """Runs built for four blocks, pack and unpack told the staging buffer holds three: the run
+    staged past the end is skipped and flagged (KV_DERR_STAGE); the other runs still move."""
+    g = W.CacheGeom("separate", 16, 16, heads, 64)  # heads * 128 B rows; 8 or 16 KiB blocks
+    rng = np.random.default_rng(31)
+    src = W.to_device_bf16(W.host_cache_tensors(g, 1, rng), "cuda")
+    dst = W.to_device_bf16(W.host_cache_tensors(g, 1, rng), "cuda")
+    dst_before = dst[0].clone()
+    scache, dcache = K.PagedCache.from_tensors(src, "separate"), K.PagedCache.from_tensors(dst, "separate")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    off, ids = W.csr([[3, 4], [9, 10]])
+    dids = np.array([1, 2, 6, 7], dtype=np.int32)
+    x = K.kv_build_xfer_list(t(off), t(ids), t(dids), 1)  # cap 1: one run per block, staged 0..3
+    K.kv_get_last_error(clear=True)
+    stage = K.kv_pack_blocks(scache, x, 3)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error(clear=True) & K.KV_DERR_STAGE
+    blk = g.block_payload_bytes
+    s_bytes = src[0].view(torch.uint8).reshape(g.num_blocks, blk)
+    np.testing.assert_array_equal(stage.cpu().numpy().reshape(3, blk), s_bytes[[3, 4, 9]].cpu().numpy())
+    K.kv_unpack_blocks(dcache, stage, x, 3, g.block_size, g.row_bytes, 0)
+    torch.cuda.synchronize()
+    assert K.kv_get_last_error(clear=True) & K.KV_DERR_STAGE
+    want = dst_before.view(torch.uint8).reshape(g.num_blocks, blk).clone()
+    want[[1, 2, 6]] = s_bytes[[3, 4, 9]]
+    np.testing.assert_array_equal(dst[0].view(torch.uint8).reshape(g.num_blocks, blk).cpu().numpy(), want.cpu().numpy())
+
+
 def test_empty_remap_step():
     """A remap step (another block size on the receiver) whose requests are all empty: every call
     succeeds and nothing is written, although the empty destination list reaches the library as a
