@@ -27,6 +27,7 @@ def test_bench_json_line():
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3 and d["higher_is_better"] is True
     assert d["config"]["workload"] == "tiny" and d["value"] > 0
+    assert d["config"]["l2"].startswith("flushed")  # a step this small is timed with L2 flushed between steps
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
