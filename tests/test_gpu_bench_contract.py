@@ -40,3 +40,21 @@ def test_bench_json_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 5 * 5  # slot_mapping, reshape_and_cache, builder, pack, unpack per step
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+@pytest.mark.parametrize("flags", [["--stage", "host"], ["--sw-window", "24"], ["--workload", "mid", "--layers", "1",
+                                                                            "--num-blocks", "2048"]],
+                         ids=["host_staging", "sliding_window", "mid_shrunk"])
+def test_bench_modes_print_one_line(flags):
+    args = [sys.executable, "bench.py", "--steps", "3", "--warmup", "3", "--no-cpu-baseline"]
+    if "--workload" not in flags:
+        args += ["--workload", "tiny"]
+    r = subprocess.run(args + flags, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["value"] > 0 and d["roofline"]["achieved"] > 0 and d["gpu_launches"] > 0
+    if "--stage" in flags:
+        assert d["config"]["stage"] == "pinned host memory" and "host_link" in d
