@@ -336,8 +336,10 @@ int check_stage(const kv_stage_desc *stage, const void *buf, int64_t stage_bytes
         (stage->n_planes != 1 && stage->n_planes != 2) || stage->slice_bytes <= 0 || stage_bytes < 0)
         return KV_ERR_INVALID_ARG;
     if (!pkv::aligned16((int64_t)stage->slice_bytes)) return KV_ERR_ALIGN;
-    const int64_t need = stage->n_blocks * stage->n_tensors * stage->n_planes * (int64_t)stage->block_size *
-                         stage->slice_bytes;
+    int64_t need = stage->n_blocks;  // staged bytes; a size past int64 is refused, not wrapped
+    const int64_t factors[4] = {stage->n_tensors, stage->n_planes, stage->block_size, stage->slice_bytes};
+    for (const int64_t f : factors)
+        if (__builtin_mul_overflow(need, f, &need)) return KV_ERR_RANGE;
     if (need > 0 && buf == nullptr) return KV_ERR_INVALID_ARG;
     if (!pkv::aligned16(buf)) return KV_ERR_ALIGN;
     if (stage_bytes < need) return KV_ERR_RANGE;

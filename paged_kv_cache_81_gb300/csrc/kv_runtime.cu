@@ -56,6 +56,14 @@ int check_cache(const kv_cache_desc *c)
     if (!aligned16((int64_t)c->row_bytes) || !aligned16(c->block_stride) || !aligned16(c->token_stride) ||
         (c->n_planes == 2 && !aligned16(c->plane_stride)))
         return KV_ERR_ALIGN;
+    // every row's byte offset, block * block_stride + plane * plane_stride + slot * token_stride
+    // + row_bytes, must fit in int64 (the kernels compute it so)
+    int64_t span = 0, part = 0;
+    if (__builtin_mul_overflow(c->num_blocks, c->block_stride, &span) ||
+        __builtin_mul_overflow((int64_t)c->block_size, c->token_stride, &part) || __builtin_add_overflow(span, part, &span) ||
+        __builtin_add_overflow(span, c->n_planes == 2 ? c->plane_stride : (int64_t)0, &span) ||
+        __builtin_add_overflow(span, (int64_t)c->row_bytes, &span))
+        return KV_ERR_RANGE;
     for (int32_t t = 0; t < c->n_tensors; t++) {
         if (c->base[t] == 0) return KV_ERR_INVALID_ARG;
         if (c->base[t] & 15u) return KV_ERR_ALIGN;

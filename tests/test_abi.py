@@ -78,6 +78,10 @@ def test_host_validation_without_gpu(lib):
     assert _pack(lib, _desc([0x1000]), K.stage_desc(4, 1, 2, 16, 24)) == K.KV_ERR_ALIGN  # slice size
     # zero work is a no-op that needs no device
     assert _pack(lib, _desc([0x1000]), K.stage_desc(0, 1, 2, 16, 256)) == K.KV_OK
+    # byte counts that do not fit in int64 are refused, not wrapped past the size checks
+    assert _pack(lib, _desc([0x1000]), K.stage_desc(1 << 60, 1, 2, 16, 256), stage_bytes=(1 << 63) - 1) == \
+        K.KV_ERR_RANGE
+    assert _pack(lib, _desc([0x1000], num_blocks=1 << 60), sd) == K.KV_ERR_RANGE
     # unpack: whole-block mode needs equal block sizes; remap mode needs both CSRs
     d = _desc([0x1000])
     bad_bs = K.stage_desc(4, 1, 2, 8, 256)
