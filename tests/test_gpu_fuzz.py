@@ -53,8 +53,8 @@ def fuzz_workload(seed: int) -> tuple:
         src_layout, dst_layout = rng.choice(["blocks_first", "kv_first"], size=2)
     else:
         src_layout = dst_layout = str(rng.choice(["separate", "mla"]))
-    bs = int(rng.choice([1, 2, 3, 8, 16]))
-    head_dim = int(rng.choice([8, 16, 24, 64]))
+    bs = int(rng.choice([1, 2, 3, 8, 16, 32]))
+    head_dim = int(rng.choice([8, 16, 24, 64, 128]))
     heads = 1 if src_layout == "mla" else int(rng.integers(1, 5))
     row = heads * head_dim * 2
     slice_off, slice_bytes = 0, 0

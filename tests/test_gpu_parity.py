@@ -173,6 +173,23 @@ def test_pack_layouts(layout, sl):
     assert K.kv_get_last_error() == 0
 
 
+@pytest.mark.parametrize("layout,heads", [("kv_first", 8), ("blocks_first", 4)],
+                         ids=["kv_first_16KiB_planes_spans", "blocks_first_16KiB_blocks_merged"])
+def test_tma_engine_layouts(layout, heads):
+    """Whole steps whose contiguous pieces reach 16 KiB, so pack and unpack take the TMA bulk
+    engine: kv-first planes of 16 KiB (SPANS: one bulk copy per plane of a block) and
+    blocks-first blocks of 16 KiB (MERGED), against the oracle."""
+    from dataclasses import replace
+    g = W.CacheGeom(layout, 64, 16, heads, 64)
+    assert g.block_payload_bytes // (g.n_planes if layout == "kv_first" else 1) >= 16 * 1024
+    wl = replace(W.TINY, name=f"tma_{layout}", src=g, dst=g)
+    case = W.make_case(wl)
+    src, dst, new = G.host_inputs(wl, case, seed=wl.seed + 41)
+    gpu = G.run_gpu(wl, case, src, dst, new)
+    ora = G.run_oracle(wl, case, src, dst, new, gpu["max_run_blocks"])
+    G.compare(gpu, ora, wl.name)
+
+
 def test_pack_unpack_strided_blocks():
     """BLOCKS mode: each block contiguous, blocks further apart than their size (a padded view)."""
     nb, bs, heads, hd = 30, 8, 2, 16
