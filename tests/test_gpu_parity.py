@@ -499,6 +499,51 @@ def test_write_tokens_large_batch(with_slot_out):
         np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
 
 
+@pytest.mark.parametrize("entry", ["reshape", "write_slot_out", "write"])
+def test_decode_write_one_wave(entry):
+    """A decode step of 256 tokens into 61 latent-layout layers (576 bf16 per row, 18 CTAs a layer:
+    1098 CTAs, a wave and a tail on 152 SMs).  Padding tokens (slot -1), a table hole and a
+    partial last CTA are included; every tensor is compared with the oracle's slot_mapping +
+    reshape_and_cache, and slot_out when it is asked for."""
+    g = W.CacheGeom("mla", 8, 64, 1, 576)
+    nt, T = 61, 256
+    rng = np.random.default_rng(95)
+    table = rng.permutation(g.num_blocks).astype(np.int32).reshape(4, 2)
+    table[3, 1] = -1  # a hole: tokens of request 3 past position 63 have no block
+    token_req = rng.integers(0, 4, T).astype(np.int32)
+    token_pos = np.empty(T, dtype=np.int32)
+    for r in range(4):  # distinct positions per request, so slots are distinct
+        k = int((token_req == r).sum())
+        token_pos[token_req == r] = rng.choice(128, size=k, replace=False)
+    want_slot, bad = oracle.slot_mapping(table, token_req, token_pos, g.block_size)
+    src = W.host_cache_tensors(g, nt, rng)
+    new = [W.normal_bf16_bytes(rng, T * g.row_bytes // 2).reshape(T, g.row_bytes // 2) for _ in range(nt)]
+    s_dev = W.to_device_bf16(src, "cuda")
+    n_dev = [x.reshape(T, 1, g.row_bytes // 2) for x in W.to_device_bf16(new, "cuda")]
+    cache = K.PagedCache.from_tensors(s_dev, "mla")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    K.kv_get_last_error(clear=True)
+    if entry == "reshape":
+        slot = want_slot.copy()
+        slot[::37] = -1  # padding tokens are skipped
+        K.kv_reshape_and_cache(cache, n_dev, t(slot))
+        torch.cuda.synchronize()
+        assert K.kv_get_last_error() == 0
+    else:
+        assert bad > 0
+        slot = want_slot
+        out = torch.full((T,), -7, dtype=torch.int64, device="cuda") if entry == "write_slot_out" else None
+        K.kv_write_tokens(cache, n_dev, t(table), t(token_req), t(token_pos), out)
+        torch.cuda.synchronize()
+        assert K.kv_get_last_error() & K.KV_DERR_TABLE
+        if out is not None:
+            np.testing.assert_array_equal(out.cpu().numpy(), want_slot)
+    sc = H.ora_cache(g, [a.copy() for a in src])
+    assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], slot) == 0
+    for a, b in zip(s_dev, sc.tensors):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+
+
 def test_write_tokens_invalid_tokens():
     g = W.CacheGeom("separate", 8, 4, 1, 64)
     host = W.host_cache_tensors(g, 1, np.random.default_rng(2))
