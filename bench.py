@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--num-blocks", type=int, default=None, help="override blocks per tensor (profiling captures)")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="host->device streams the e2e leg splits each step's new rows over")
+    ap.add_argument("--write-only", action="store_true",
+                    help="only the new-token write (slot_mapping + reshape_and_cache, kv_write_tokens); no receiver "
+                         "or staging buffer (profiling captures)")
     ap.add_argument("--hash-only", action="store_true",
                     help="run only the prefix-hash measurement (kv_block_hashes), e.g. to profile its kernels")
     return ap.parse_args()
@@ -564,9 +567,40 @@ def measure_write_path(step, dev, iters: int = 200) -> dict:
     graph = step.capture(step.write_tokens_fused)
     fused_replay = timed(graph.replay)
     del graph
+    device = measure_write_device({"two_calls": step.write_tokens, "write_tokens": step.write_tokens_fused}, dev)
     return {"tokens": step.n_tokens, "tensors": len(step.src.tensors), "eager_us_per_step": round(eager, 2),
             "graph_us_per_step": round(replay, 2), "fused_eager_us_per_step": round(fused_eager, 2),
-            "fused_graph_us_per_step": round(fused_replay, 2)}
+            "fused_graph_us_per_step": round(fused_replay, 2), "device_us_per_write_back_to_back": device}
+
+
+def measure_write_device(fns: dict, dev, per_graph: int = 20, replays: int = 10) -> dict:
+    """Device time of one new-token write issued back to back: `per_graph` writes captured in one
+    CUDA graph, the graph replayed `replays` times between CUDA events on the replaying stream."""
+    import torch
+
+    cur = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    out = {}
+    for name, fn in fns.items():
+        fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        side.wait_stream(cur)
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(per_graph):
+                fn()
+        cur.wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for _ in range(replays):
+            g.replay()
+        b.record(cur)
+        torch.cuda.synchronize(dev)
+        out[name] = round(a.elapsed_time(b) * 1e3 / (replays * per_graph), 2)
+        del g
+    return out
 
 
 def measure_host_link(host_buf, dev, stream, reps: int = 5) -> dict:
@@ -876,10 +910,57 @@ def run_hash_only(args):
                                                                              reps=args.steps)}), flush=True)
 
 
+def run_write_only(args):
+    """Only the new-token write of the workload: the source cache and the new rows are allocated,
+    no receiver cache or staging buffer.  The driver for profiling the write kernels: it issues
+    `--steps` eager rounds of slot_mapping + reshape_and_cache and of kv_write_tokens (without
+    slot_out), then (unless --no-extras) times each from CUDA graphs."""
+    import torch
+    from paged_kv_cache_81_gb300 import build
+    build.build()
+    from paged_kv_cache_81_gb300 import pagedkv as K
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workload(args)
+    case = W.make_case(wl)
+    if not case.n_tokens:
+        raise SystemExit(f"workload {wl.name} writes no new tokens")
+    seed = wl.seed * 7919
+    cache = K.PagedCache.from_tensors(W.device_cache(wl.src, wl.n_tensors, dev, seed=seed), wl.src.layout)
+    new = W.new_token_rows(wl.src, wl.n_tensors, case.n_tokens, dev, seed=seed + 2)
+    table, req, pos = (torch.from_numpy(a).to(dev) for a in (case.block_table, case.token_req, case.token_pos))
+    slot = torch.empty(case.n_tokens, dtype=torch.int64, device=dev)
+    bs = wl.src.block_size
+
+    def two_calls():
+        K.kv_slot_mapping(table, req, pos, bs, slot)
+        K.kv_reshape_and_cache(cache, new, slot)
+
+    def write_tokens():
+        K.kv_write_tokens(cache, new, table, req, pos, None)
+
+    K.kv_get_last_error(clear=True)
+    for _ in range(args.steps):
+        two_calls()
+        write_tokens()
+    torch.cuda.synchronize(dev)
+    err = K.kv_get_last_error()
+    if err:
+        raise SystemExit(f"device error word {err:#x}")
+    line = {"workload": wl.name, "tokens": case.n_tokens, "tensors": wl.n_tensors,
+            "bytes_per_write": 2 * case.n_tokens * wl.src.n_planes * wl.src.row_bytes * wl.n_tensors}
+    if not args.no_extras:
+        line["device_us_per_write_back_to_back"] = measure_write_device(
+            {"two_calls": two_calls, "write_tokens": write_tokens}, dev)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.hash_only:
         run_hash_only(args)
+    elif args.write_only:
+        run_write_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -4,6 +4,8 @@
 // block = slots 0..15 of K/V rows: label "Paged kv cache"; one block_table serves every
 // layer: label "总的就是 all kv cache".
 #include <algorithm>
+#include <climits>
+#include <numeric>
 
 #include "kv_common.cuh"
 
@@ -60,6 +62,8 @@ struct ReshapeParams {
     FastDiv div_bs;
     FastDiv div_tokens;
     int32_t n_planes;
+    uint32_t n_tokens;
+    uint32_t tok_step;   // reshape_rows_kernel: the grid stride in tokens
     int *err;
     uint64_t dst[pkv::kMaxTensorsPerLaunch];
     uint64_t src[pkv::kMaxTensorsPerLaunch * 2];
@@ -78,6 +82,9 @@ struct ReshapeParams {
 #define PKV_RESHAPE_PLANE_MAJOR 0  // 1: order work (plane, token, chunk) instead of (token, plane, chunk)
 #endif
 constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
+#ifndef PKV_RESHAPE_ROWS
+#define PKV_RESHAPE_ROWS 1  // 0: every row write takes the general kernel
+#endif
 #ifndef PKV_WRITE_SPLIT_ITERATIONS
 #define PKV_WRITE_SPLIT_ITERATIONS 2  // kv_write_tokens: grid-stride iterations per thread above which it splits
 #endif
@@ -163,6 +170,64 @@ __global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
     }
 }
 
+// The row write when the grid stride is a whole number of tokens (a multiple of planes x
+// chunks per row): then every row a thread takes has the thread's first plane and chunk and
+// the rows' tokens are tok_step apart, so the coordinates are computed once per thread and
+// each row costs one address step.  Each pass issues its row loads, then all their slot
+// lookups, then the stores: a load placed after a store cannot be moved above it (the compiler
+// must assume they may alias), so interleaving them would make each row's lookup (two
+// dependent loads when FUSED) wait for the previous row's store.
+template <bool FUSED>
+__global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
+    reshape_rows_kernel(const __grid_constant__ ReshapeParams p)
+{
+    constexpr int64_t kNoRow = INT64_MIN;  // past the last token
+    const int t = blockIdx.y;
+    const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t row0 = pkv::fdiv(first, p.div_cpr);
+    const uint32_t chunk = first - row0 * p.div_cpr.d;
+    const uint32_t tok0 = pkv::fdiv(row0, p.div_planes);  // >= n_tokens when first is past the work
+    const uint32_t plane = row0 - tok0 * p.div_planes.d;
+    const uint8_t *const src = reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane]) + chunk * 16;
+    uint8_t *const dst = reinterpret_cast<uint8_t *>(p.dst[t]) + (int64_t)plane * p.plane_stride + chunk * 16;
+    const bool reporter = FUSED && t == 0 && plane == 0 && chunk == 0;  // one thread per token reports
+    for (uint32_t tok = tok0; tok < p.n_tokens; tok += p.tok_step * kReshapeUnroll) {
+        uint4 v[kReshapeUnroll];
+        int64_t s[kReshapeUnroll];
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            const uint32_t tk = tok + u * p.tok_step;
+            if (tk < p.n_tokens) v[u] = pkv::ld_once(src + (int64_t)tk * p.src_token_stride);
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            const uint32_t tk = tok + u * p.tok_step;
+            s[u] = kNoRow;
+            if (tk < p.n_tokens) s[u] = FUSED ? table_slot(p, tk) : p.slot[tk];
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            if (s[u] == kNoRow) continue;
+            if (FUSED) {
+                if (reporter && p.slot_out != nullptr) p.slot_out[tok + u * p.tok_step] = s[u];
+                if (s[u] < 0) {
+                    if (reporter) pkv::set_error(p.err, KV_DERR_TABLE);
+                    continue;
+                }
+            } else if (s[u] < 0) {
+                continue;  // padding token
+            }
+            if (s[u] >= (int64_t)p.slot_limit) {
+                pkv::set_error(p.err, KV_DERR_SLOT);
+                continue;
+            }
+            const uint32_t block = pkv::fdiv((uint32_t)s[u], p.div_bs);
+            const uint32_t off = (uint32_t)s[u] - block * p.div_bs.d;
+            pkv::st_stream(dst + (int64_t)block * p.block_stride + (int64_t)off * p.token_stride, v[u]);
+        }
+    }
+}
+
 // Argument checks of a row write (kv_reshape_and_cache, kv_write_tokens).  KV_OK with
 // *nothing = true when there is nothing to launch.
 int validate_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride, int64_t n_tokens,
@@ -191,6 +256,7 @@ int validate_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t ne
 }
 
 constexpr int kRowThreads = 256;
+constexpr int64_t kMaxRowGroup = 16;
 
 // CTAs per tensor of a row-write launch: enough for the work, at most about four waves of
 // 8 resident CTAs per SM over the nt tensors of the launch.
@@ -227,7 +293,11 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
     p.div_bs = pkv::make_fastdiv((uint32_t)cache->block_size);
     p.div_tokens = pkv::make_fastdiv((uint32_t)n_tokens);
     p.n_planes = cache->n_planes;
+    p.n_tokens = (uint32_t)n_tokens;
     p.err = dev->err_word;
+    // CTAs a grid stride must be a multiple of to cover whole tokens (planes x chunks per row
+    // divides 256 x CTAs); above kMaxRowGroup the general kernel runs instead.
+    const int64_t row_group = cache->n_planes * cpr / std::gcd<int64_t>(kRowThreads, cache->n_planes * cpr);
 
     int64_t *slot_out = p.slot_out;
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
@@ -240,8 +310,14 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
         p.slot_out = t0 == 0 ? slot_out : nullptr;
         int64_t per_tensor_ctas, cap;
         row_grid(cache, n_tokens, nt, *dev, &per_tensor_ctas, &cap);
-        const dim3 grid((unsigned)std::min(per_tensor_ctas, cap), (unsigned)nt);
-        reshape_and_cache_kernel<FUSED><<<grid, kRowThreads, 0, stream>>>(p);
+        int64_t ctas = std::min(per_tensor_ctas, cap);
+        if (PKV_RESHAPE_ROWS && row_group <= kMaxRowGroup) {
+            ctas = (ctas + row_group - 1) / row_group * row_group;
+            p.tok_step = (uint32_t)(ctas * kRowThreads / (cache->n_planes * cpr));
+            reshape_rows_kernel<FUSED><<<dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream>>>(p);
+        } else {
+            reshape_and_cache_kernel<FUSED><<<dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream>>>(p);
+        }
         st = pkv::cuda_status(cudaGetLastError());
         if (st != KV_OK) return st;
     }

@@ -58,3 +58,18 @@ def test_bench_modes_print_one_line(flags):
     assert d["value"] > 0 and d["roofline"]["achieved"] > 0 and d["gpu_launches"] > 0
     if "--stage" in flags:
         assert d["config"]["stage"] == "pinned host memory" and "host_link" in d
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+@pytest.mark.parametrize("workload,extra", [("tiny", []), ("mla", ["--num-blocks", "512"])], ids=["tiny", "mla_small"])
+def test_bench_write_only(workload, extra):
+    """--write-only (the write kernels' profiling driver) prints one line with both write forms timed."""
+    r = subprocess.run([sys.executable, "bench.py", "--write-only", "--workload", workload, "--steps", "3"] + extra,
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["tokens"] > 0 and d["bytes_per_write"] > 0
+    assert set(d["device_us_per_write_back_to_back"]) == {"two_calls", "write_tokens"}
+    assert all(v > 0 for v in d["device_us_per_write_back_to_back"].values())

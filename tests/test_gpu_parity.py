@@ -544,6 +544,52 @@ def test_decode_write_one_wave(entry):
         np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["reshape", "write_tokens"])
+@pytest.mark.parametrize("layout,hd", [("separate", 136), ("blocks_first", 136), ("mla", 200), ("mla", 288),
+                                       ("kv_first", 24), ("mla", 8)],
+                         ids=["sep_17_chunks", "bf_2x17_chunks", "mla_25_chunks", "mla_36_chunks", "kvf_2x3_chunks",
+                              "mla_1_chunk"])
+def test_row_write_chunk_counts(layout, hd, fused):
+    """Row writes whose chunk count per token (planes x 16-byte chunks of a row) does or does not
+    divide a whole number of 256-thread CTAs within 16 CTAs: 17, 34 and 25 chunks take the general
+    kernel, 36, 6 and 1 the token-strided one.  Token counts leave ragged tails; padding tokens
+    (slot -1) are skipped."""
+    g = W.CacheGeom(layout, 24, 8, 1, hd)
+    rng = np.random.default_rng(hd + len(layout))
+    src = W.host_cache_tensors(g, 3, rng)
+    T = 70
+    table = rng.permutation(g.num_blocks).astype(np.int32).reshape(3, 8)
+    token_req = rng.integers(0, 3, T).astype(np.int32)
+    token_pos = np.empty(T, dtype=np.int32)
+    for r in range(3):
+        k = int((token_req == r).sum())
+        token_pos[token_req == r] = rng.choice(64, size=k, replace=False)
+    want_slot, bad = oracle.slot_mapping(table, token_req, token_pos, g.block_size)
+    assert bad == 0
+    new = [W.normal_bf16_bytes(rng, T * g.row_bytes // 2).reshape(T, g.row_bytes // 2)
+           for _ in range(3 * g.n_planes)]
+    s_dev = W.to_device_bf16(src, "cuda")
+    n_dev = [x.reshape(G._new_shape(g, T)) for x in W.to_device_bf16(new, "cuda")]
+    cache = K.PagedCache.from_tensors(s_dev, layout)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    K.kv_get_last_error(clear=True)
+    slot = want_slot.copy()
+    if fused:
+        out = torch.full((T,), -7, dtype=torch.int64, device="cuda")
+        K.kv_write_tokens(cache, n_dev, t(table), t(token_req), t(token_pos), out)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.cpu().numpy(), want_slot)
+    else:
+        slot[::9] = -1
+        K.kv_reshape_and_cache(cache, n_dev, t(slot))
+        torch.cuda.synchronize()
+    assert K.kv_get_last_error() == 0
+    sc = H.ora_cache(g, [a.copy() for a in src])
+    assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], slot) == 0
+    for a, b in zip(s_dev, sc.tensors):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
+
+
 def test_write_tokens_invalid_tokens():
     g = W.CacheGeom("separate", 8, 4, 1, 64)
     host = W.host_cache_tensors(g, 1, np.random.default_rng(2))
