@@ -20,6 +20,9 @@
  *    pointer table) are read during the call only.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and never synchronises, except kv_get_last_error.
+ *  - Kernels are launched with programmatic stream serialisation allowed, so their CTAs may
+ *    be scheduled while the previous kernel on `stream` still runs; each waits for that
+ *    kernel to complete before its first memory access, so the data sees plain stream order.
  *  - Payload bytes are opaque: rows are moved as 16-byte vectors and never converted,
  *    so NaN payloads, infinities and -0 arrive bit-exact.
  *  - Argument errors the host can see are returned at once and nothing is launched.

@@ -170,6 +170,7 @@ struct Pipe {
 template <bool MERGE, bool PACK>
 __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_constant__ CopyParams p)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
@@ -287,7 +288,7 @@ int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo 
             configured[di][m][d] = true;
         }
     }
-    fn<<<dev.num_sms * per_sm[di][m][d], kPipes * 32, kSmemBytes, s>>>(p);
+    pkv::launch(fn, dev.num_sms * per_sm[di][m][d], kPipes * 32, kSmemBytes, s, p);
     return cuda_status(cudaGetLastError());
 }
 

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kScanThreads) clip_count_kernel(const int32_t 
                                                                   int32_t n_ids, const int32_t *__restrict__ n_tokens,
                                                                   int32_t window, int32_t bs, int32_t *out_off, int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     __shared__ int32_t warp_sum[kScanThreads / 32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(256) clip_copy_kernel(const int32_t *__restric
                                                         int32_t bs, const int32_t *__restrict__ out_off,
                                                         int32_t *__restrict__ out_ids, int64_t out_capacity, int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     const int32_t step = gridDim.x * blockDim.x;
     for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n_ids; i += step) {
         int32_t lo = 0, hi = n_reqs - 1;  // last request whose first entry is <= i
@@ -126,13 +128,13 @@ extern "C" int kv_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, c
     if (dev == nullptr) return KV_ERR_CUDA;
     const cudaStream_t s = (cudaStream_t)stream;
     if (n_reqs == 0) return pkv::cuda_status(cudaMemsetAsync(out_offsets, 0, sizeof(int32_t), s));
-    clip_count_kernel<<<1, kScanThreads, 0, s>>>(req_offsets, n_reqs, (int32_t)n_ids, n_tokens, window, block_size,
+    pkv::launch(clip_count_kernel, 1, kScanThreads, 0, s, req_offsets, n_reqs, (int32_t)n_ids, n_tokens, window, block_size,
                                                   out_offsets, dev->err_word);
     int st = pkv::cuda_status(cudaGetLastError());
     if (st != KV_OK || n_ids == 0) return st;
     const int threads = 256;
     const int blocks = (int)std::min<int64_t>((n_ids + threads - 1) / threads, (int64_t)dev->num_sms * 8);
-    clip_copy_kernel<<<blocks, threads, 0, s>>>(req_offsets, n_reqs, ids, (int32_t)n_ids, n_tokens, window,
+    pkv::launch(clip_copy_kernel, blocks, threads, 0, s, req_offsets, n_reqs, ids, (int32_t)n_ids, n_tokens, window,
                                                 block_size, out_offsets, out_ids, out_capacity, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }

@@ -84,6 +84,43 @@ __device__ __forceinline__ void set_error(int *err, int bits)
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with programmatic
+// stream serialisation allowed, so its CTAs may be scheduled while the previous kernel on the
+// stream is still running.  Each kernel therefore calls grid_dep_entry() before its first
+// global memory access: griddepcontrol.wait returns once every prerequisite grid has completed
+// and its memory operations are visible (at once when there is none), which keeps plain stream
+// order for the data; only launch and CTA setup overlap the previous kernel.  The kernel then
+// allows its own dependents to be scheduled (they take effect once all its CTAs have started).
+// ---------------------------------------------------------------------------
+#ifndef PKV_PDL
+#define PKV_PDL 1  // 0: plain stream-ordered launches
+#endif
+
+__device__ __forceinline__ void grid_dep_entry()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// cudaLaunchKernelEx with programmatic stream serialisation (when PKV_PDL is on).
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // Host-side runtime state (kv_runtime.cu).
 // ---------------------------------------------------------------------------
 struct DeviceInfo {

@@ -51,6 +51,7 @@ template <int MODE, bool PACK>
 __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTAS : PKV_COPY_MIN_CTAS)
     copy_runs_kernel(const __grid_constant__ CopyParams p)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -322,7 +323,7 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
         if (bulk) {
             st = pkv::launch_bulk_copy(p, mode, pack, *dev, s);
         } else {
-            fn<<<grid, kThreads, 0, s>>>(p);
+            pkv::launch(fn, grid, kThreads, 0, s, p);
             st = pkv::cuda_status(cudaGetLastError());
         }
         if (st != KV_OK) return st;

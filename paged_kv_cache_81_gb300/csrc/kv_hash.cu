@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t 
                                                                   int32_t n_tokens, int32_t bs, int32_t *out_off,
                                                                   int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     __shared__ int32_t warp_sum[kScanThreads / 32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kChainThreads) hash_chain_kernel(const int32_t
                                                                    uint64_t *__restrict__ out, int64_t out_capacity,
                                                                    int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < n_reqs; r += gridDim.x * blockDim.x) {
         int32_t begin, k;
         int64_t at;
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
                                                                    const int32_t *__restrict__ out_off,
                                                                    uint64_t *__restrict__ table, int64_t limit)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     __shared__ uint32_t sh_tok[kTableChunk];
     __shared__ SplitWeight sh_w[kTableChunkBytes];
     const int64_t n_hash = min((int64_t)out_off[n_reqs], limit);
@@ -297,6 +300,7 @@ __global__ void __launch_bounds__(32) hash_walk_kernel(const int32_t *__restrict
                                                        const uint64_t *__restrict__ table, int64_t limit,
                                                        uint64_t *__restrict__ out, int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     constexpr int kGroups = kRing / kBatch;  // commit groups in flight
     extern __shared__ __align__(16) uint64_t ring_mem[];  // kRing tables of 256 entries
     uint64_t(*ring)[256] = reinterpret_cast<uint64_t(*)[256]>(ring_mem);
@@ -373,13 +377,13 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
     if (dev == nullptr) return KV_ERR_CUDA;
     const cudaStream_t s = (cudaStream_t)stream;
     if (n_reqs == 0) return pkv::cuda_status(cudaMemsetAsync(out_offsets, 0, sizeof(int32_t), s));
-    hash_count_kernel<<<1, kScanThreads, 0, s>>>(tok_offsets, n_reqs, (int32_t)n_tokens, block_size, out_offsets,
+    pkv::launch(hash_count_kernel, 1, kScanThreads, 0, s, tok_offsets, n_reqs, (int32_t)n_tokens, block_size, out_offsets,
                                                   dev->err_word);
     int st = pkv::cuda_status(cudaGetLastError());
     if (st != KV_OK) return st;
     if (workspace == nullptr) {
         const int blocks = std::max(1, std::min((n_reqs + kChainThreads - 1) / kChainThreads, dev->num_sms * 4));
-        hash_chain_kernel<<<blocks, kChainThreads, 0, s>>>(tok_offsets, n_reqs, tokens, (int32_t)n_tokens, block_size,
+        pkv::launch(hash_chain_kernel, blocks, kChainThreads, 0, s, tok_offsets, n_reqs, tokens, (int32_t)n_tokens, block_size,
                                                            seed, out_offsets, out_hashes, out_capacity, dev->err_word);
         return pkv::cuda_status(cudaGetLastError());
     }
@@ -388,7 +392,7 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
     if (limit == 0) return KV_OK;
     uint64_t *table = reinterpret_cast<uint64_t *>(workspace);
     const int table_blocks = (int)std::min<int64_t>(limit, (int64_t)dev->num_sms * 8);
-    hash_table_kernel<<<table_blocks, kTableThreads, 0, s>>>(tok_offsets, n_reqs, tokens, (int32_t)n_tokens,
+    pkv::launch(hash_table_kernel, table_blocks, kTableThreads, 0, s, tok_offsets, n_reqs, tokens, (int32_t)n_tokens,
                                                              block_size, out_offsets, table, limit);
     st = pkv::cuda_status(cudaGetLastError());
     if (st != KV_OK) return st;
@@ -406,7 +410,7 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
         }
     }
     const int walk_blocks = std::min(n_reqs, dev->num_sms * 16);
-    hash_walk_kernel<<<walk_blocks, 32, kRingBytes, s>>>(tok_offsets, n_reqs, (int32_t)n_tokens, block_size, seed, p_pow_n,
+    pkv::launch(hash_walk_kernel, walk_blocks, 32, kRingBytes, s, tok_offsets, n_reqs, (int32_t)n_tokens, block_size, seed, p_pow_n,
                                                 out_offsets, table, limit, out_hashes, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }

@@ -27,6 +27,7 @@ __device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p)
 
 __global__ void post_signal_kernel(kv_signal *signal, uint64_t add)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     __threadfence();
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(&signal->value), "l"(add) : "memory");
 }
@@ -36,6 +37,7 @@ __global__ void post_signal_kernel(kv_signal *signal, uint64_t add)
 __global__ void wait_signal_kernel(const kv_signal *signal, uint64_t expected, uint64_t timeout_ns, int32_t *status,
                                    int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     const unsigned long long t0 = now_ns();
     unsigned ns = 64;
     while (true) {
@@ -59,7 +61,7 @@ namespace pkv {
 
 int post_signal(kv_signal *signal, uint64_t add, cudaStream_t s)
 {
-    post_signal_kernel<<<1, 1, 0, s>>>(signal, add);
+    pkv::launch(post_signal_kernel, 1, 1, 0, s, signal, add);
     return cuda_status(cudaGetLastError());
 }
 
@@ -73,7 +75,7 @@ extern "C" int kv_wait_signal(const kv_signal *signal, uint64_t expected, uint32
     if (timeout_us == 0 || timeout_us > kMaxTimeoutUs) return KV_ERR_RANGE;
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
-    wait_signal_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(signal, expected, (uint64_t)timeout_us * 1000ull,
+    pkv::launch(wait_signal_kernel, 1, 1, 0, (cudaStream_t)stream, signal, expected, (uint64_t)timeout_us * 1000ull,
                                                           status_out, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }

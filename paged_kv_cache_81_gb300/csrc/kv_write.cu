@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(const int32_t *__rest
                                                            int32_t block_size, int64_t *__restrict__ slot,
                                                            int *err)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_tokens; i += step) {
         const int32_t req = token_req[i];
@@ -108,6 +109,7 @@ template <bool FUSED>
 __global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
     reshape_and_cache_kernel(const __grid_constant__ ReshapeParams p)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     const int t = blockIdx.y;
     uint8_t *const dst = reinterpret_cast<uint8_t *>(p.dst[t]);
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -181,6 +183,7 @@ template <bool FUSED>
 __global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
     reshape_rows_kernel(const __grid_constant__ ReshapeParams p)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     constexpr int64_t kNoRow = INT64_MIN;  // past the last token
     const int t = blockIdx.y;
     const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
@@ -314,9 +317,9 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
         if (PKV_RESHAPE_ROWS && row_group <= kMaxRowGroup) {
             ctas = (ctas + row_group - 1) / row_group * row_group;
             p.tok_step = (uint32_t)(ctas * kRowThreads / (cache->n_planes * cpr));
-            reshape_rows_kernel<FUSED><<<dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream>>>(p);
+            pkv::launch(reshape_rows_kernel<FUSED>, dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream, p);
         } else {
-            reshape_and_cache_kernel<FUSED><<<dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream>>>(p);
+            pkv::launch(reshape_and_cache_kernel<FUSED>, dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream, p);
         }
         st = pkv::cuda_status(cudaGetLastError());
         if (st != KV_OK) return st;
@@ -344,7 +347,7 @@ int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t max_bloc
     const int threads = 256;
     const int64_t need = (n_tokens + threads - 1) / threads;
     const int blocks = (int)std::min<int64_t>(need, (int64_t)dev->num_sms * 16);
-    slot_mapping_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(
+    pkv::launch(slot_mapping_kernel, blocks, threads, 0, (cudaStream_t)stream,
         block_table, n_reqs, max_blocks_per_req, bt_row_stride, token_req, token_pos, n_tokens, block_size,
         slot_out, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());

@@ -315,6 +315,7 @@ __device__ __forceinline__ int32_t resolve_and_write(const XferParams &p, const 
 
 __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_constant__ XferParams p)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     __shared__ int32_t sh_scan[kWarps];
     __shared__ int32_t sh_tile;
     __shared__ Pre sh_pre;
@@ -472,6 +473,7 @@ constexpr int kSWarps = kSThreads / 32;
 
 __global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __grid_constant__ XferParams p)
 {
+    pkv::grid_dep_entry();  // before any global memory access
     __shared__ int32_t sh_src[kSTile + 2];
     __shared__ int32_t sh_dst[kSTile + 2];
     __shared__ int32_t sh_off[kOffsetCache];
@@ -539,7 +541,7 @@ int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *sr
                 configured[dev.device & 63] = true;
             }
         }
-        build_xfer_single_kernel<<<1, kSThreads, kSingleRecordBytes, s>>>(p);
+        pkv::launch(build_xfer_single_kernel, 1, kSThreads, kSingleRecordBytes, s, p);
         return pkv::cuda_status(cudaGetLastError());
     }
     const int st = pkv::cuda_status(cudaMemsetAsync(scratch, 0, (size_t)need, s));
@@ -547,6 +549,8 @@ int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *sr
     p.counter = reinterpret_cast<uint32_t *>(scratch);
     p.tiles = reinterpret_cast<TileRecord *>(reinterpret_cast<uint8_t *>(scratch) + kHeaderBytes);
     const int tiles = (int)((n_blocks + kTile - 1) / kTile);
+    // A plain stream-ordered launch: the scratch memset just before it is not a kernel that
+    // the entry wait would cover.
     build_xfer_kernel<<<tiles, kThreads, 0, s>>>(p);
     return pkv::cuda_status(cudaGetLastError());
 }
