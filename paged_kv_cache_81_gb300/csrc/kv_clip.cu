@@ -128,13 +128,13 @@ extern "C" int kv_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, c
     if (dev == nullptr) return KV_ERR_CUDA;
     const cudaStream_t s = (cudaStream_t)stream;
     if (n_reqs == 0) return pkv::cuda_status(cudaMemsetAsync(out_offsets, 0, sizeof(int32_t), s));
-    pkv::launch(clip_count_kernel, 1, kScanThreads, 0, s, req_offsets, n_reqs, (int32_t)n_ids, n_tokens, window, block_size,
-                                                  out_offsets, dev->err_word);
+    pkv::launch(clip_count_kernel, 1, kScanThreads, 0, s, req_offsets, n_reqs, (int32_t)n_ids, n_tokens, window,
+                block_size, out_offsets, dev->err_word);
     int st = pkv::cuda_status(cudaGetLastError());
     if (st != KV_OK || n_ids == 0) return st;
     const int threads = 256;
     const int blocks = (int)std::min<int64_t>((n_ids + threads - 1) / threads, (int64_t)dev->num_sms * 8);
     pkv::launch(clip_copy_kernel, blocks, threads, 0, s, req_offsets, n_reqs, ids, (int32_t)n_ids, n_tokens, window,
-                                                block_size, out_offsets, out_ids, out_capacity, dev->err_word);
+                block_size, out_offsets, out_ids, out_capacity, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }

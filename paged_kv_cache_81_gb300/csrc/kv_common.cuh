@@ -102,8 +102,9 @@ __device__ __forceinline__ void grid_dep_entry()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// cudaLaunchKernelEx with programmatic stream serialisation (when PKV_PDL is on).
-template <typename... KArgs, typename... Args>
+// cudaLaunchKernelEx with programmatic stream serialisation (when PKV_PDL is on and Pdl is true;
+// launch<false> is a plain stream-ordered launch).
+template <bool Pdl = true, typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                    Args &&...args)
 {
@@ -114,7 +115,7 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL;
+    attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL && Pdl;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);

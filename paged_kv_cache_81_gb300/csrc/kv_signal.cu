@@ -76,6 +76,6 @@ extern "C" int kv_wait_signal(const kv_signal *signal, uint64_t expected, uint32
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
     pkv::launch(wait_signal_kernel, 1, 1, 0, (cudaStream_t)stream, signal, expected, (uint64_t)timeout_us * 1000ull,
-                                                          status_out, dev->err_word);
+                status_out, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }

@@ -347,9 +347,8 @@ int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t max_bloc
     const int threads = 256;
     const int64_t need = (n_tokens + threads - 1) / threads;
     const int blocks = (int)std::min<int64_t>(need, (int64_t)dev->num_sms * 16);
-    pkv::launch(slot_mapping_kernel, blocks, threads, 0, (cudaStream_t)stream,
-        block_table, n_reqs, max_blocks_per_req, bt_row_stride, token_req, token_pos, n_tokens, block_size,
-        slot_out, dev->err_word);
+    pkv::launch(slot_mapping_kernel, blocks, threads, 0, (cudaStream_t)stream, block_table, n_reqs, max_blocks_per_req,
+                bt_row_stride, token_req, token_pos, n_tokens, block_size, slot_out, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }
 
