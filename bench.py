@@ -544,9 +544,11 @@ def measure_single_request(step, dev, blocks: int = 64, iters: int = 200):
 
 
 def measure_write_path(step, dev, iters: int = 200) -> dict:
-    """Wall-clock cost of the new-token write (kv_slot_mapping + kv_reshape_and_cache) issued
-    call by call from Python and replayed from a CUDA graph; the same for kv_write_tokens, the
-    two calls fused into one launch."""
+    """Wall-clock cost of the new-token write issued call by call from Python and replayed from a
+    CUDA graph, in three forms: kv_slot_mapping + kv_reshape_and_cache; kv_write_tokens with
+    slot_out (the same two kernels behind one call); kv_write_tokens without slot_out (the slot
+    lookup fused into the row copy, one launch).  Plus each form's device time per write issued
+    back to back from a graph."""
     import torch
 
     def timed(fn):
@@ -559,18 +561,16 @@ def measure_write_path(step, dev, iters: int = 200) -> dict:
         torch.cuda.synchronize(dev)
         return (time.perf_counter() - t0) / iters * 1e6
 
-    eager = timed(step.write_tokens)
-    graph = step.capture(step.write_tokens)
-    replay = timed(graph.replay)
-    del graph
-    fused_eager = timed(step.write_tokens_fused)
-    graph = step.capture(step.write_tokens_fused)
-    fused_replay = timed(graph.replay)
-    del graph
-    device = measure_write_device({"two_calls": step.write_tokens, "write_tokens": step.write_tokens_fused}, dev)
-    return {"tokens": step.n_tokens, "tensors": len(step.src.tensors), "eager_us_per_step": round(eager, 2),
-            "graph_us_per_step": round(replay, 2), "fused_eager_us_per_step": round(fused_eager, 2),
-            "fused_graph_us_per_step": round(fused_replay, 2), "device_us_per_write_back_to_back": device}
+    forms = {"": step.write_tokens, "write_tokens_": step.write_tokens_call, "fused_": step.write_tokens_fused}
+    out = {"tokens": step.n_tokens, "tensors": len(step.src.tensors)}
+    for prefix, fn in forms.items():
+        out[f"{prefix}eager_us_per_step"] = round(timed(fn), 2)
+        graph = step.capture(fn)
+        out[f"{prefix}graph_us_per_step"] = round(timed(graph.replay), 2)
+        del graph
+    out["device_us_per_write_back_to_back"] = measure_write_device(
+        {"two_calls": step.write_tokens, "write_tokens": step.write_tokens_call, "fused": step.write_tokens_fused}, dev)
+    return out
 
 
 def measure_write_device(fns: dict, dev, per_graph: int = 20, replays: int = 10) -> dict:
@@ -913,8 +913,8 @@ def run_hash_only(args):
 def run_write_only(args):
     """Only the new-token write of the workload: the source cache and the new rows are allocated,
     no receiver cache or staging buffer.  The driver for profiling the write kernels: it issues
-    `--steps` eager rounds of slot_mapping + reshape_and_cache and of kv_write_tokens (without
-    slot_out), then (unless --no-extras) times each from CUDA graphs."""
+    `--steps` eager rounds of slot_mapping + reshape_and_cache and of kv_write_tokens without
+    slot_out (the fused kernel), then (unless --no-extras) times each from CUDA graphs."""
     import torch
     from paged_kv_cache_81_gb300 import build
     build.build()
@@ -936,13 +936,13 @@ def run_write_only(args):
         K.kv_slot_mapping(table, req, pos, bs, slot)
         K.kv_reshape_and_cache(cache, new, slot)
 
-    def write_tokens():
+    def fused():
         K.kv_write_tokens(cache, new, table, req, pos, None)
 
     K.kv_get_last_error(clear=True)
     for _ in range(args.steps):
         two_calls()
-        write_tokens()
+        fused()
     torch.cuda.synchronize(dev)
     err = K.kv_get_last_error()
     if err:
@@ -951,7 +951,7 @@ def run_write_only(args):
             "bytes_per_write": 2 * case.n_tokens * wl.src.n_planes * wl.src.row_bytes * wl.n_tensors}
     if not args.no_extras:
         line["device_us_per_write_back_to_back"] = measure_write_device(
-            {"two_calls": two_calls, "write_tokens": write_tokens}, dev)
+            {"two_calls": two_calls, "fused": fused}, dev)
     print(json.dumps(line), flush=True)
 
 

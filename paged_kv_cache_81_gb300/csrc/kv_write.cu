@@ -87,7 +87,7 @@ constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
 #define PKV_RESHAPE_ROWS 1  // 0: every row write takes the general kernel
 #endif
 #ifndef PKV_WRITE_SPLIT_ITERATIONS
-#define PKV_WRITE_SPLIT_ITERATIONS 2  // kv_write_tokens: grid-stride iterations per thread above which it splits
+#define PKV_WRITE_SPLIT_ITERATIONS 0  // kv_write_tokens with slot_out: grid-stride passes per thread above which it splits
 #endif
 constexpr int64_t kWriteSplitIterations = PKV_WRITE_SPLIT_ITERATIONS;
 
@@ -371,10 +371,10 @@ int kv_write_tokens(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t 
                          (n_reqs > 0 && max_blocks_per_req > 0 && block_table == nullptr)))
         return KV_ERR_INVALID_ARG;
     if (n_reqs > 0 && bt_row_stride < max_blocks_per_req) return KV_ERR_INVALID_ARG;
-    // A large batch walks several grid-stride iterations per thread, and in the fused kernel
-    // each waits on the table lookup's dependent loads.  With slot_out given, such a batch
-    // runs as slot_mapping into slot_out followed by the plain row copy: the same results,
-    // one extra launch.
+    // In the fused kernel every pass of a thread waits on the table lookup's two dependent
+    // loads.  With slot_out given, the batch runs as slot_mapping into slot_out followed by the
+    // plain row copy instead: the same results, and the row copy's launch overlaps slot_mapping
+    // (programmatic dependent launch), so it is faster for a decode write too.
     bool nothing = false;
     int st = validate_rows(cache, new_kv, new_token_stride, n_tokens, &nothing);
     if (st != KV_OK || nothing) return st;

@@ -94,12 +94,20 @@ class TransferStep:
         K.kv_slot_mapping(self.block_table, self.token_req, self.token_pos, self.src.block_size, self.slot, stream)
         K.kv_reshape_and_cache(self.src, self.new_kv, self.slot, stream)
 
-    def write_tokens_fused(self, stream=None):
-        """The same write as write_tokens with the slot lookup fused into the row copy (one launch)."""
+    def write_tokens_call(self, stream=None):
+        """The same write as write_tokens through the one call kv_write_tokens, slots kept (it runs
+        the two kernels, the second launch overlapping the first)."""
         if not self.n_tokens:
             return
         K.kv_write_tokens(self.src, self.new_kv, self.block_table, self.token_req, self.token_pos, self.slot,
                           stream)
+
+    def write_tokens_fused(self, stream=None):
+        """The same cache write through kv_write_tokens without slot_out: the slot lookup fused into
+        the row copy (one launch); the slots are not kept."""
+        if not self.n_tokens:
+            return
+        K.kv_write_tokens(self.src, self.new_kv, self.block_table, self.token_req, self.token_pos, None, stream)
 
     @staticmethod
     def kept_blocks(case: Case, window: int, block_size: int) -> int:

@@ -71,5 +71,5 @@ def test_bench_write_only(workload, extra):
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["tokens"] > 0 and d["bytes_per_write"] > 0
-    assert set(d["device_us_per_write_back_to_back"]) == {"two_calls", "write_tokens"}
+    assert set(d["device_us_per_write_back_to_back"]) == {"two_calls", "fused"}
     assert all(v > 0 for v in d["device_us_per_write_back_to_back"].values())

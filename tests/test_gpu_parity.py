@@ -442,24 +442,27 @@ def test_staging_guard_canaries(wl):
     np.testing.assert_array_equal(b[guard:guard + n], want)
 
 
+@pytest.mark.parametrize("with_slot_out", [True, False], ids=["two_launches", "fused"])
 @pytest.mark.parametrize("wl", [W.TINY, W.small(W.MLA), W.small(W.PAGE), W.small(W.PAGE_KV_FIRST)],
                          ids=lambda w: w.name)
-def test_write_tokens_fused_matches_oracle(wl):
-    """kv_write_tokens (slot lookup fused into the row copy) == oracle slot_mapping + reshape_and_cache."""
+def test_write_tokens_matches_oracle(wl, with_slot_out):
+    """kv_write_tokens == oracle slot_mapping + reshape_and_cache: with slot_out (slot_mapping, then
+    the row copy) and without (the slot lookup fused into the row copy)."""
     case = W.make_case(wl)
     src, _, new = G.host_inputs(wl, case, seed=wl.seed + 17)
     s_dev = W.to_device_bf16(src, "cuda")
     n_dev = [x.reshape(G._new_shape(wl.src, case.n_tokens)) for x in W.to_device_bf16(new, "cuda")]
     cache = K.PagedCache.from_tensors(s_dev, wl.src.layout)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
-    slot = torch.full((case.n_tokens,), -7, dtype=torch.int64, device="cuda")
+    slot = torch.full((case.n_tokens,), -7, dtype=torch.int64, device="cuda") if with_slot_out else None
     K.kv_get_last_error(clear=True)
     K.kv_write_tokens(cache, n_dev, t(case.block_table), t(case.token_req), t(case.token_pos), slot)
     torch.cuda.synchronize()
     assert K.kv_get_last_error() == 0
     want_slot, bad = oracle.slot_mapping(case.block_table, case.token_req, case.token_pos, wl.src.block_size)
     assert bad == 0
-    np.testing.assert_array_equal(slot.cpu().numpy(), want_slot)
+    if with_slot_out:
+        np.testing.assert_array_equal(slot.cpu().numpy(), want_slot)
     sc = H.ora_cache(wl.src, [a.copy() for a in src])
     assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], want_slot) == 0
     for a, b in zip(s_dev, sc.tensors):
@@ -468,8 +471,9 @@ def test_write_tokens_fused_matches_oracle(wl):
 
 @pytest.mark.parametrize("with_slot_out", [True, False], ids=["split", "fused"])
 def test_write_tokens_large_batch(with_slot_out):
-    """A prefill large enough that kv_write_tokens runs slot_mapping and the row copy as two
-    launches when it may write slot_out; without slot_out the same batch stays fused."""
+    """A 48-layer prefill of 8192 tokens through kv_write_tokens: slot_mapping and the row copy as
+    two launches when it may write slot_out; without slot_out the fused kernel, several grid-stride
+    passes per thread."""
     g = W.CacheGeom("blocks_first", 1024, 16, 1, 128)
     wl = W.Workload("write_large", 90, "page", n_layers=48, src=g, dst=g)
     rng = np.random.default_rng(91)
@@ -544,16 +548,17 @@ def test_decode_write_one_wave(entry):
         np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b)
 
 
-@pytest.mark.parametrize("fused", [False, True], ids=["reshape", "write_tokens"])
+@pytest.mark.parametrize("entry", ["reshape", "write_tokens", "fused"])
 @pytest.mark.parametrize("layout,hd", [("separate", 136), ("blocks_first", 136), ("mla", 200), ("mla", 288),
                                        ("kv_first", 24), ("mla", 8)],
                          ids=["sep_17_chunks", "bf_2x17_chunks", "mla_25_chunks", "mla_36_chunks", "kvf_2x3_chunks",
                               "mla_1_chunk"])
-def test_row_write_chunk_counts(layout, hd, fused):
+def test_row_write_chunk_counts(layout, hd, entry):
     """Row writes whose chunk count per token (planes x 16-byte chunks of a row) does or does not
     divide a whole number of 256-thread CTAs within 16 CTAs: 17, 34 and 25 chunks take the general
     kernel, 36, 6 and 1 the token-strided one.  Token counts leave ragged tails; padding tokens
-    (slot -1) are skipped."""
+    (slot -1) are skipped.  Entries: kv_reshape_and_cache, kv_write_tokens with slot_out (two
+    launches) and without (the fused kernel)."""
     g = W.CacheGeom(layout, 24, 8, 1, hd)
     rng = np.random.default_rng(hd + len(layout))
     src = W.host_cache_tensors(g, 3, rng)
@@ -574,11 +579,12 @@ def test_row_write_chunk_counts(layout, hd, fused):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     K.kv_get_last_error(clear=True)
     slot = want_slot.copy()
-    if fused:
-        out = torch.full((T,), -7, dtype=torch.int64, device="cuda")
+    if entry != "reshape":
+        out = torch.full((T,), -7, dtype=torch.int64, device="cuda") if entry == "write_tokens" else None
         K.kv_write_tokens(cache, n_dev, t(table), t(token_req), t(token_pos), out)
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(out.cpu().numpy(), want_slot)
+        if out is not None:
+            np.testing.assert_array_equal(out.cpu().numpy(), want_slot)
     else:
         slot[::9] = -1
         K.kv_reshape_and_cache(cache, n_dev, t(slot))
