@@ -457,34 +457,43 @@ __global__ void __launch_bounds__(kThreads) build_xfer_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Single-CTA builder for lists that fit one tile of kSTile entries: the look-back kernel
+// Single-CTA builder for lists that fit one tile of NT * kSItems entries: the look-back kernel
 // without the look-back, so it needs neither the scratch nor its zeroing.  A short list
 // (a decode-side request, a few prompts) is then one launch.  Longer lists go to the
 // look-back kernel: one CTA walking several tiles in turn is slower than one CTA per tile.
-// The run records go through kSTile * 24 bytes of dynamic shared memory (see below).
+// The run records go through NT * kSItems * 24 bytes of dynamic shared memory (see below).
+// Lists of up to kSSmallTile entries (one request's blocks, say) take a 128-thread instance,
+// which needs 15 KB of records instead of 123 KB and fits beside other work on any SM.
 // ---------------------------------------------------------------------------
 #ifndef PKV_XFER_SINGLE_ITEMS
 #define PKV_XFER_SINGLE_ITEMS 5
 #endif
+#ifndef PKV_XFER_SMALL_THREADS
+#define PKV_XFER_SMALL_THREADS 128  // 0: every single-tile list takes the 1024-thread instance
+#endif
 constexpr int kSThreads = 1024;
 constexpr int kSItems = PKV_XFER_SINGLE_ITEMS;
 constexpr int kSTile = kSThreads * kSItems;
-constexpr int kSWarps = kSThreads / 32;
+constexpr int kSSmallThreads = PKV_XFER_SMALL_THREADS > 0 ? PKV_XFER_SMALL_THREADS : 32;
+constexpr int kSSmallTile = PKV_XFER_SMALL_THREADS > 0 ? kSSmallThreads * kSItems : 0;
 
-__global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __grid_constant__ XferParams p)
+template <int NT>
+__global__ void __launch_bounds__(NT) build_xfer_single_kernel(const __grid_constant__ XferParams p)
 {
     pkv::grid_dep_entry();  // before any global memory access
-    __shared__ int32_t sh_src[kSTile + 2];
-    __shared__ int32_t sh_dst[kSTile + 2];
+    constexpr int kTileN = NT * kSItems;
+    constexpr int kNW = NT / 32;
+    __shared__ int32_t sh_src[kTileN + 2];
+    __shared__ int32_t sh_dst[kTileN + 2];
     __shared__ int32_t sh_off[kOffsetCache];
-    __shared__ int32_t sh_scan[kSWarps];
+    __shared__ int32_t sh_scan[kNW];
 
     const int tid = threadIdx.x;
     const int32_t o_first = tid == 0 ? __ldg(p.req_offsets) : 0;  // the offsets' ends, checked below
     const int32_t o_last = tid == 0 ? __ldg(p.req_offsets + p.n_reqs) : p.n;
     bool nat[kSItems + 1];
     int32_t req[kSItems];
-    stage_and_mark<kSItems, kSThreads>(p, 0, sh_src, sh_dst, sh_off, nat, req);
+    stage_and_mark<kSItems, NT>(p, 0, sh_src, sh_dst, sh_off, nat, req);
     if (o_first != 0 || o_last != p.n) pkv::set_error(p.err, KV_DERR_LIST);
     const int32_t i0 = tid * kSItems;
     int32_t my_last = -1;
@@ -493,17 +502,17 @@ __global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __gr
         if (i0 + k < p.n && nat[k]) my_last = i0 + k;
     int32_t unused;
     // natural start open at i0; -1 only when the offsets do not start at 0
-    const int32_t s0 = block_exclusive<kSWarps>(my_last, -1, Max(), sh_scan, &unused);
+    const int32_t s0 = block_exclusive<kNW>(my_last, -1, Max(), sh_scan, &unused);
     // records go to shared memory first: one thread's runs are consecutive records, so direct
     // stores from a thread's items scatter over a whole warp's range of sectors
-    extern __shared__ __align__(16) kv_xfer_run sh_rec[];  // kSTile records
-    const int32_t cnt = resolve_and_write<kSItems, kSWarps>(p, nat, req, i0, 0, p.n, s0, 0, sh_src, sh_dst, sh_scan,
-                                                            KV_DERR_LIST, sh_rec);
+    extern __shared__ __align__(16) kv_xfer_run sh_rec[];  // kTileN records
+    const int32_t cnt = resolve_and_write<kSItems, kNW>(p, nat, req, i0, 0, p.n, s0, 0, sh_src, sh_dst, sh_scan,
+                                                        KV_DERR_LIST, sh_rec);
     __syncthreads();
     const int64_t n_out = min((int64_t)cnt, p.capacity);  // records past the capacity are not written
     const unsigned long long *src64 = reinterpret_cast<const unsigned long long *>(sh_rec);
     unsigned long long *dst64 = reinterpret_cast<unsigned long long *>(p.runs);
-    for (int64_t w = tid; w < n_out * 3; w += kSThreads) dst64[w] = src64[w];
+    for (int64_t w = tid; w < n_out * 3; w += NT) dst64[w] = src64[w];
     if (tid == 0) {
         *p.n_runs = cnt;
         if ((int64_t)cnt > p.capacity) pkv::set_error(p.err, KV_DERR_CAPACITY);
@@ -511,6 +520,8 @@ __global__ void __launch_bounds__(kSThreads) build_xfer_single_kernel(const __gr
 }
 
 constexpr int kSingleRecordBytes = kSTile * (int)sizeof(kv_xfer_run);
+constexpr int kSmallRecordBytes = kSSmallTile * (int)sizeof(kv_xfer_run);
+static_assert(kSmallRecordBytes <= 48 * 1024, "the small builder's records must fit the default dynamic smem");
 
 // Launches the single-CTA builder for lists of one tile (the scratch is not touched), else zeroes the look-back scratch (tile counter and tile records: `need` bytes
 // at `scratch`) and launches one CTA per tile.
@@ -529,6 +540,10 @@ int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *sr
     p.n_reqs = n_reqs;
     p.n = (int32_t)n_blocks;
     p.cap = max_run_blocks;
+    if (n_blocks <= kSSmallTile) {
+        pkv::launch(build_xfer_single_kernel<kSSmallThreads>, 1, kSSmallThreads, kSmallRecordBytes, s, p);
+        return pkv::cuda_status(cudaGetLastError());
+    }
     if (n_blocks <= kSTile) {
         static std::mutex mu;
         static bool configured[64];
@@ -536,12 +551,12 @@ int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *sr
             std::lock_guard<std::mutex> lock(mu);
             if (!configured[dev.device & 63]) {
                 const int st = pkv::cuda_status(cudaFuncSetAttribute(
-                    build_xfer_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleRecordBytes));
+                    build_xfer_single_kernel<kSThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleRecordBytes));
                 if (st != KV_OK) return st;
                 configured[dev.device & 63] = true;
             }
         }
-        pkv::launch(build_xfer_single_kernel, 1, kSThreads, kSingleRecordBytes, s, p);
+        pkv::launch(build_xfer_single_kernel<kSThreads>, 1, kSThreads, kSingleRecordBytes, s, p);
         return pkv::cuda_status(cudaGetLastError());
     }
     const int st = pkv::cuda_status(cudaMemsetAsync(scratch, 0, (size_t)need, s));

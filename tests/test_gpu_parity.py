@@ -58,18 +58,21 @@ def _builder_case(n_reqs, lens, rng, frag=(12, 0.6), n_ids=None):
     return W.csr(W.pop_lists(q, lens))
 
 
-@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096, 5119, 5120, 5121, 6145, 20000, 100003])
+@pytest.mark.parametrize("n", [1, 64, 639, 640, 641, 2047, 2048, 2049, 4096, 5119, 5120, 5121, 6145, 20000, 100003])
 @pytest.mark.parametrize("cap", [0, 1, 2, 7, 32])
-def test_builder_tiles(n, cap):
+@pytest.mark.parametrize("req_len", [3000, 1], ids=["long_requests", "one_block_requests"])
+def test_builder_tiles(n, cap, req_len):
     """Runs across tile boundaries, long runs, empty requests, all cap variants.
 
-    Lists of up to 5120 entries go to the single-CTA builder (one tile), longer ones to the
-    look-back builder (tiles of 2048); the sizes straddle both limits and the look-back tile edges."""
-    rng = np.random.default_rng(n * 31 + cap)
+    Lists of up to 640 entries go to the 128-thread single-CTA builder, up to 5120 to the
+    1024-thread one (one tile each), longer ones to the look-back builder (tiles of 2048); the
+    sizes straddle the three limits and the look-back tile edges.  Requests are up to 3000
+    entries long, or one entry each (as many requests as entries)."""
+    rng = np.random.default_rng(n * 31 + cap + req_len)
     lens = []
     left = n
     while left > 0:
-        k = int(min(left, rng.integers(0, 3000)))
+        k = int(min(left, rng.integers(0, req_len + 1) if req_len > 1 else 1))
         lens.append(k)
         left -= k
     lens.insert(len(lens) // 2, 0)  # an empty request in the middle
