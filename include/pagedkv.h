@@ -369,6 +369,13 @@ KV_API int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_o
  * bounded: after timeout_us microseconds (1 .. 60,000,000; otherwise KV_ERR_RANGE) it gives
  * up, writes KV_ERR_TIMEOUT to *status_out (device int32, may be NULL) and sets
  * KV_DERR_TIMEOUT; on success it writes KV_OK.  The context stays usable either way.
+ * While it polls, the work that sets the counter runs on another stream, and its kernels must
+ * already be loaded: CUDA loads a kernel's code lazily, on first use, and that load may
+ * synchronise the context, which would hold the producer's launch until this wait ends.  The
+ * first call on a device loads every kernel of this library before it queues the poll; load
+ * your own producer kernels first (run them once, or set CUDA_MODULE_LOADING=EAGER).  The
+ * kernels queued after the wait on `stream` are scheduled only once it ends, so they cannot
+ * take the SM space the producer needs.
  */
 KV_API int kv_wait_signal(const kv_signal *signal, uint64_t expected, uint32_t timeout_us, int32_t *status_out,
                           kv_stream_t stream);

@@ -269,6 +269,12 @@ BulkFn pick(int mode, bool pack)
 
 namespace pkv {
 
+int preload_bulk_kernels()
+{
+    return load_kernels(bulk_copy_kernel<true, true>, bulk_copy_kernel<true, false>, bulk_copy_kernel<false, true>,
+                        bulk_copy_kernel<false, false>);
+}
+
 int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s)
 {
     static std::mutex mu;

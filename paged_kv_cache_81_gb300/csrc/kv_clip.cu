@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(256) clip_copy_kernel(const int32_t *__restric
 
 }  // namespace
 
+int pkv::preload_clip_kernels() { return pkv::load_kernels(clip_count_kernel, clip_copy_kernel); }
+
 extern "C" int kv_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, const int32_t *ids, int64_t n_ids,
                                    const int32_t *n_tokens, int32_t window, int32_t block_size,
                                    int32_t *out_offsets, int32_t *out_ids, int64_t out_capacity,

@@ -91,14 +91,18 @@ __device__ __forceinline__ void set_error(int *err, int bits)
 // and its memory operations are visible (at once when there is none), which keeps plain stream
 // order for the data; only launch and CTA setup overlap the previous kernel.  The kernel then
 // allows its own dependents to be scheduled (they take effect once all its CTAs have started).
+// A kernel that waits for work on another stream calls grid_dep_wait() alone: its dependents
+// are then scheduled only when it ends, so they cannot hold the SM space that work needs.
 // ---------------------------------------------------------------------------
 #ifndef PKV_PDL
 #define PKV_PDL 1  // 0: plain stream-ordered launches
 #endif
 
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void grid_dep_entry()
 {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    grid_dep_wait();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -146,5 +150,30 @@ int post_signal(kv_signal *signal, uint64_t add, cudaStream_t s);
 
 // Validates a cache descriptor; checks the tensor base addresses too.
 int check_cache(const kv_cache_desc *c);
+
+// Kernel preloading.  CUDA loads a kernel's code lazily, on first use, and loading may
+// synchronise the context; a launch that loads a kernel while another stream runs a kernel
+// that polls (kv_wait_signal) would then wait for that poll to end.  cudaFuncGetAttributes
+// loads a kernel, so each source file lists its kernels here, and kv_wait_signal loads them
+// all (once per device) before it queues its polling kernel.
+template <typename... Fns>
+int load_kernels(Fns... fns)
+{
+    cudaFuncAttributes attr;
+    for (const void *f : {reinterpret_cast<const void *>(fns)...}) {
+        const cudaError_t e = cudaFuncGetAttributes(&attr, f);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return KV_OK;
+}
+int preload_write_kernels();   // kv_write.cu
+int preload_xfer_kernels();    // kv_xfer.cu
+int preload_copy_kernels();    // kv_copy.cu
+int preload_bulk_kernels();    // kv_bulk.cu
+int preload_clip_kernels();    // kv_clip.cu
+int preload_hash_kernels();    // kv_hash.cu
+int preload_signal_kernels();  // kv_signal.cu
+// All of the above, once per device (kv_runtime.cu).
+int preload_all_kernels(const DeviceInfo &dev);
 
 }  // namespace pkv

@@ -349,6 +349,13 @@ int check_stage(const kv_stage_desc *stage, const void *buf, int64_t stage_bytes
 
 }  // namespace
 
+int pkv::preload_copy_kernels()
+{
+    return pkv::load_kernels(copy_runs_kernel<MERGED, true>, copy_runs_kernel<MERGED, false>,
+                             copy_runs_kernel<SPANS, true>, copy_runs_kernel<SPANS, false>, copy_runs_kernel<ROWS, true>,
+                             copy_runs_kernel<ROWS, false>, copy_runs_kernel<REMAP, false>);
+}
+
 extern "C" {
 
 int kv_pack_blocks(const kv_cache_desc *src, int32_t src_slice_off, const kv_stage_desc *stage,

@@ -361,6 +361,11 @@ __global__ void __launch_bounds__(32) hash_walk_kernel(const int32_t *__restrict
 
 }  // namespace
 
+int pkv::preload_hash_kernels()
+{
+    return pkv::load_kernels(hash_count_kernel, hash_chain_kernel, hash_table_kernel, hash_walk_kernel);
+}
+
 extern "C" int kv_block_hashes_workspace_bytes(int64_t n_tokens, int32_t block_size, int64_t *bytes_out)
 {
     if (bytes_out == nullptr || n_tokens < 0 || block_size <= 0) return KV_ERR_INVALID_ARG;

@@ -71,6 +71,21 @@ int check_cache(const kv_cache_desc *c)
     return KV_OK;
 }
 
+int preload_all_kernels(const DeviceInfo &dev)
+{
+    static std::mutex mu;
+    static bool done[kMaxDevices];
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev.device]) return KV_OK;
+    for (int (*load)() : {preload_write_kernels, preload_xfer_kernels, preload_copy_kernels, preload_bulk_kernels,
+                          preload_clip_kernels, preload_hash_kernels, preload_signal_kernels}) {
+        const int st = load();
+        if (st != KV_OK) return st;
+    }
+    done[dev.device] = true;
+    return KV_OK;
+}
+
 }  // namespace pkv
 
 extern "C" {

@@ -37,7 +37,10 @@ __global__ void post_signal_kernel(kv_signal *signal, uint64_t add)
 __global__ void wait_signal_kernel(const kv_signal *signal, uint64_t expected, uint64_t timeout_ns, int32_t *status,
                                    int *err)
 {
-    pkv::grid_dep_entry();  // before any global memory access
+    // The entry wait only: the kernels queued after this one must not be scheduled while it polls,
+    // or a persistent copy grid among them could take the SM space of the work on another stream
+    // that sets the counter, and the wait would run out.
+    pkv::grid_dep_wait();
     const unsigned long long t0 = now_ns();
     unsigned ns = 64;
     while (true) {
@@ -59,6 +62,8 @@ __global__ void wait_signal_kernel(const kv_signal *signal, uint64_t expected, u
 
 namespace pkv {
 
+int preload_signal_kernels() { return load_kernels(post_signal_kernel, wait_signal_kernel); }
+
 int post_signal(kv_signal *signal, uint64_t add, cudaStream_t s)
 {
     pkv::launch(post_signal_kernel, 1, 1, 0, s, signal, add);
@@ -75,6 +80,9 @@ extern "C" int kv_wait_signal(const kv_signal *signal, uint64_t expected, uint32
     if (timeout_us == 0 || timeout_us > kMaxTimeoutUs) return KV_ERR_RANGE;
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
+    // every kernel of the library is loaded before the poll starts (see preload_all_kernels)
+    const int st = pkv::preload_all_kernels(*dev);
+    if (st != KV_OK) return st;
     pkv::launch(wait_signal_kernel, 1, 1, 0, (cudaStream_t)stream, signal, expected, (uint64_t)timeout_us * 1000ull,
                 status_out, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());

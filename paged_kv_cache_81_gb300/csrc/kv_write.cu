@@ -329,6 +329,12 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
 
 }  // namespace
 
+int pkv::preload_write_kernels()
+{
+    return pkv::load_kernels(slot_mapping_kernel, reshape_and_cache_kernel<true>, reshape_and_cache_kernel<false>,
+                             reshape_rows_kernel<true>, reshape_rows_kernel<false>);
+}
+
 extern "C" {
 
 int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t max_blocks_per_req,

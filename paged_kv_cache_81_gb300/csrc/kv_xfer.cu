@@ -572,6 +572,12 @@ int launch_builder(const int32_t *req_offsets, int32_t n_reqs, const int32_t *sr
 
 }  // namespace
 
+int pkv::preload_xfer_kernels()
+{
+    return pkv::load_kernels(build_xfer_single_kernel<kSSmallThreads>, build_xfer_single_kernel<kSThreads>,
+                             build_xfer_kernel);
+}
+
 extern "C" {
 
 int kv_xfer_workspace_bytes(int64_t n_blocks, int64_t *bytes_out)

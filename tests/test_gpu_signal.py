@@ -8,6 +8,11 @@ or waits on a counter nothing sets and must time out, reporting KV_ERR_TIMEOUT.
 """
 from __future__ import annotations
 
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -108,3 +113,78 @@ def test_wait_argument_checks():
     assert lib.kv_wait_signal(K._ptr(sig), 1, 60_000_001, None, K._stream()) == K.KV_ERR_RANGE
     assert lib.kv_wait_signal(ctypes.c_void_p(sig.data_ptr() + 8), 1, 10, None, K._stream()) == K.KV_ERR_ALIGN
     assert lib.kv_wait_signal(None, 1, 10, None, K._stream()) == K.KV_ERR_INVALID_ARG
+
+
+def test_wait_then_copy_leaves_room_for_the_producer():
+    """Stream A waits for a counter that a signalled unpack on stream B sets, then packs: a
+    persistent grid that fills every SM.  The pack must not be scheduled while the wait polls, or
+    it would hold the SM space the unpack needs and the wait would run out.  B starts late (a
+    sleep kernel), so A's wait is already polling when the unpack is queued.  The pack reads the
+    blocks the unpack wrote, ordered by the counter, and must return the staged bytes."""
+    n, bs, row = 40, 16, 256
+    g = W.CacheGeom("separate", 256, bs, 1, row // 2)  # 4 KiB blocks: the register-staged engine
+    rng = np.random.default_rng(31)
+    cache = K.PagedCache.from_tensors(W.device_cache(g, 2, "cuda", seed=31), "separate")
+    ids = rng.permutation(256)[:n].astype(np.int32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    off = t([0, n])
+    x_in = K.kv_build_xfer_list(off, t(ids), t(ids), 0)  # runs carry the ids as destination blocks
+    x_out = K.kv_build_xfer_list(off, t(ids), None, 0)
+    stage_in = torch.from_numpy(rng.integers(0, 256, size=2 * n * bs * row, dtype=np.uint8)).cuda()
+    stage_out = torch.zeros_like(stage_in)
+    sig = K.new_signal()
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda._sleep(1000)  # the sleep kernel is this test's own producer-side kernel: load it before the poll
+    torch.cuda.synchronize()
+    K.kv_get_last_error(clear=True)
+    with torch.cuda.stream(a):
+        status = K.kv_wait_signal(sig, 1, 2_000_000)
+        K.kv_pack_blocks(cache, x_out, n, stage_out)
+    with torch.cuda.stream(b):
+        torch.cuda._sleep(50_000_000)
+        K.kv_unpack_blocks(cache, stage_in, x_in, n, bs, signal=sig, signal_add=1)
+    torch.cuda.synchronize()
+    assert int(status.item()) == K.KV_OK
+    assert K.kv_get_last_error() == 0
+    assert torch.equal(stage_out, stage_in)
+
+
+_FRESH_PROCESS = r"""
+import json, sys
+import numpy as np, torch
+sys.path.insert(0, ".")
+from paged_kv_cache_81_gb300 import pagedkv as K
+from paged_kv_cache_81_gb300 import workloads as W
+K.load()
+n, bs, row = 40, 16, 256
+g = W.CacheGeom("separate", 256, bs, 1, row // 2)
+rng = np.random.default_rng(32)
+cache = K.PagedCache.from_tensors(W.device_cache(g, 2, "cuda", seed=32), "separate")
+ids = rng.permutation(256)[:n].astype(np.int32)
+t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+x = K.kv_build_xfer_list(t([0, n]), t(ids), t(ids), 0)
+stage_in = torch.from_numpy(rng.integers(0, 256, size=2 * n * bs * row, dtype=np.uint8)).cuda()
+sig = K.new_signal()
+a, b = torch.cuda.Stream(), torch.cuda.Stream()
+torch.cuda.synchronize()
+with torch.cuda.stream(a):
+    status = K.kv_wait_signal(sig, 1, 2_000_000)
+with torch.cuda.stream(b):  # the unpack kernel's first use in this process
+    K.kv_unpack_blocks(cache, stage_in, x, n, bs, signal=sig, signal_add=1)
+torch.cuda.synchronize()
+got = torch.stack([c.view(torch.uint8).reshape(256, -1)[torch.from_numpy(ids.astype(np.int64)).cuda()]
+                   for c in cache.tensors]).reshape(-1)
+print(json.dumps({"status": int(status.item()), "err": K.kv_get_last_error(),
+                  "data_ok": bool(torch.equal(got, stage_in))}))
+"""
+
+
+def test_wait_does_not_hold_a_producer_kernel_loaded_after_it():
+    """In a fresh process, queue a wait on stream A, then the first signalled unpack of the
+    process on stream B.  The unpack's kernel must already be loaded: loading it while the wait
+    polls may synchronise the context, which would hold the unpack until the wait runs out."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH_PROCESS], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d == {"status": K.KV_OK, "err": 0, "data_ok": True}
