@@ -174,12 +174,12 @@ KV_API int kv_reshape_and_cache(const kv_cache_desc *cache, const uint64_t *new_
 
 /*
  * kv_write_tokens [S "batch tensor 组装", "Paged kv cache"]: kv_slot_mapping and
- * kv_reshape_and_cache in one call.  With slot_out given it runs the two kernels (slot_mapping
- * into slot_out, then the plain row copy, whose launch overlaps the first); without it, each
- * token's slot is looked up in the block table inside the row-copy kernel (block_size =
- * cache->block_size), one kernel per 128 tensors.  The fused lookup adds two dependent loads
- * to every pass of the copy, which costs more than the second launch on both a decode write
- * and a prefill.  Arguments as for the two calls; slot_out (device
+ * kv_reshape_and_cache in one call.  Each token's slot is looked up in the block table inside
+ * the row-copy kernel (block_size = cache->block_size), one launch per 128 tensors, and
+ * written to slot_out when it is given.  A row shape whose n_planes * row_bytes / 16 chunks
+ * need more than 16 CTAs of 256 threads to span a whole number of tokens (e.g. 17 or 25
+ * chunks) takes a kernel without the pipelined lookup; with slot_out given it then runs as
+ * the two calls.  Arguments as for the two calls; slot_out (device
  * int64 [n_tokens], may be NULL) receives the slots, -1 for invalid tokens, exactly as
  * kv_slot_mapping writes them.  An invalid token sets KV_DERR_TABLE and writes nothing; a slot
  * beyond the cache sets KV_DERR_SLOT.  Limits as for kv_reshape_and_cache.

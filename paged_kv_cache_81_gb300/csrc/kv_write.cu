@@ -48,7 +48,7 @@ struct ReshapeParams {
     const int32_t *table;
     const int32_t *token_req;
     const int32_t *token_pos;
-    int64_t *slot_out;  // optional: the looked-up slots are also written here (first launch only)
+    int64_t *slot_out;  // optional, fused token-strided kernel: the looked-up slots (first launch only)
     int64_t table_row_stride;
     int32_t n_reqs;
     int32_t max_blocks;
@@ -76,6 +76,9 @@ struct ReshapeParams {
 #ifndef PKV_RESHAPE_MIN_CTAS
 #define PKV_RESHAPE_MIN_CTAS 6  // launch-bounds hint: resident CTAs per SM the register budget must allow
 #endif
+#ifndef PKV_RESHAPE_FUSED_MIN_CTAS
+#define PKV_RESHAPE_FUSED_MIN_CTAS 4  // the same hint for the fused row write (more state per row in flight)
+#endif
 #ifndef PKV_RESHAPE_LOADS_FIRST
 #define PKV_RESHAPE_LOADS_FIRST 1  // 0: resolve each row's slot before issuing its load
 #endif
@@ -86,10 +89,6 @@ constexpr int kReshapeUnroll = PKV_RESHAPE_UNROLL;
 #ifndef PKV_RESHAPE_ROWS
 #define PKV_RESHAPE_ROWS 1  // 0: every row write takes the general kernel
 #endif
-#ifndef PKV_WRITE_SPLIT_ITERATIONS
-#define PKV_WRITE_SPLIT_ITERATIONS 0  // kv_write_tokens with slot_out: grid-stride passes per thread above which it splits
-#endif
-constexpr int64_t kWriteSplitIterations = PKV_WRITE_SPLIT_ITERATIONS;
 
 // The slot of token `tok`: the block table's entry for the token's logical block times the
 // block size plus the offset in the block, or -1 for an invalid token.
@@ -146,7 +145,6 @@ __global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
             if (FUSED) {
                 s = table_slot(p, tok[u]);
                 const bool first = t == 0 && plane[u] == 0 && chunk[u] == 0;  // one thread per token reports
-                if (first && p.slot_out != nullptr) p.slot_out[tok[u]] = s;
                 if (s < 0) {
                     if (first) pkv::set_error(p.err, KV_DERR_TABLE);
                     continue;
@@ -176,57 +174,120 @@ __global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
 // chunks per row): then every row a thread takes has the thread's first plane and chunk and
 // the rows' tokens are tok_step apart, so the coordinates are computed once per thread and
 // each row costs one address step.  Each pass issues its row loads, then all their slot
-// lookups, then the stores: a load placed after a store cannot be moved above it (the compiler
-// must assume they may alias), so interleaving them would make each row's lookup (two
-// dependent loads when FUSED) wait for the previous row's store.
-template <bool FUSED>
-__global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS)
-    reshape_rows_kernel(const __grid_constant__ ReshapeParams p)
+// loads, then the stores: a load placed after a store cannot be moved above it (the compiler
+// must assume they may alias), so interleaving them would make each row's slot load wait for
+// the previous row's store.
+struct RowCoords {
+    const uint8_t *src;  // the thread's chunk of token 0's row
+    uint8_t *dst;        // the thread's chunk of the row at slot 0 of block 0
+    uint32_t tok0;       // the thread's first token (>= n_tokens when the thread has no work)
+    bool reporter;       // tensor 0, plane 0, chunk 0: the one thread per token that reports
+};
+
+__device__ __forceinline__ RowCoords row_coords(const ReshapeParams &p)
 {
-    pkv::grid_dep_entry();  // before any global memory access
-    constexpr int64_t kNoRow = INT64_MIN;  // past the last token
     const int t = blockIdx.y;
     const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
     const uint32_t row0 = pkv::fdiv(first, p.div_cpr);
     const uint32_t chunk = first - row0 * p.div_cpr.d;
-    const uint32_t tok0 = pkv::fdiv(row0, p.div_planes);  // >= n_tokens when first is past the work
+    const uint32_t tok0 = pkv::fdiv(row0, p.div_planes);
     const uint32_t plane = row0 - tok0 * p.div_planes.d;
-    const uint8_t *const src = reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane]) + chunk * 16;
-    uint8_t *const dst = reinterpret_cast<uint8_t *>(p.dst[t]) + (int64_t)plane * p.plane_stride + chunk * 16;
-    const bool reporter = FUSED && t == 0 && plane == 0 && chunk == 0;  // one thread per token reports
-    for (uint32_t tok = tok0; tok < p.n_tokens; tok += p.tok_step * kReshapeUnroll) {
+    return RowCoords{reinterpret_cast<const uint8_t *>(p.src[t * p.n_planes + plane]) + chunk * 16,
+                     reinterpret_cast<uint8_t *>(p.dst[t]) + (int64_t)plane * p.plane_stride + chunk * 16, tok0,
+                     t == 0 && plane == 0 && chunk == 0};
+}
+
+__global__ void __launch_bounds__(256, PKV_RESHAPE_MIN_CTAS) reshape_rows_kernel(const __grid_constant__ ReshapeParams p)
+{
+    pkv::grid_dep_entry();  // before any global memory access
+    constexpr int64_t kNoRow = INT64_MIN;  // past the last token
+    const RowCoords rc = row_coords(p);
+    for (uint32_t tok = rc.tok0; tok < p.n_tokens; tok += p.tok_step * kReshapeUnroll) {
         uint4 v[kReshapeUnroll];
         int64_t s[kReshapeUnroll];
 #pragma unroll
         for (int u = 0; u < kReshapeUnroll; u++) {
             const uint32_t tk = tok + u * p.tok_step;
-            if (tk < p.n_tokens) v[u] = pkv::ld_once(src + (int64_t)tk * p.src_token_stride);
+            if (tk < p.n_tokens) v[u] = pkv::ld_once(rc.src + (int64_t)tk * p.src_token_stride);
         }
 #pragma unroll
         for (int u = 0; u < kReshapeUnroll; u++) {
             const uint32_t tk = tok + u * p.tok_step;
-            s[u] = kNoRow;
-            if (tk < p.n_tokens) s[u] = FUSED ? table_slot(p, tk) : p.slot[tk];
+            s[u] = tk < p.n_tokens ? p.slot[tk] : kNoRow;
         }
 #pragma unroll
         for (int u = 0; u < kReshapeUnroll; u++) {
-            if (s[u] == kNoRow) continue;
-            if (FUSED) {
-                if (reporter && p.slot_out != nullptr) p.slot_out[tok + u * p.tok_step] = s[u];
-                if (s[u] < 0) {
-                    if (reporter) pkv::set_error(p.err, KV_DERR_TABLE);
-                    continue;
-                }
-            } else if (s[u] < 0) {
-                continue;  // padding token
-            }
+            if (s[u] < 0) continue;  // padding token, or past the last token
             if (s[u] >= (int64_t)p.slot_limit) {
                 pkv::set_error(p.err, KV_DERR_SLOT);
                 continue;
             }
             const uint32_t block = pkv::fdiv((uint32_t)s[u], p.div_bs);
             const uint32_t off = (uint32_t)s[u] - block * p.div_bs.d;
-            pkv::st_stream(dst + (int64_t)block * p.block_stride + (int64_t)off * p.token_stride, v[u]);
+            pkv::st_stream(rc.dst + (int64_t)block * p.block_stride + (int64_t)off * p.token_stride, v[u]);
+        }
+    }
+}
+
+// The same row write with each token's slot looked up in the block table (kv_write_tokens).
+// A slot takes two dependent loads: the token's request and position, then its table entry.
+// The first pair for the next pass is loaded during this pass, so a pass issues its row loads
+// and its table loads together and waits about one round trip, as the plain row write does.
+// The state this keeps in flight needs 64 registers: 4 CTAs per SM.
+__global__ void __launch_bounds__(256, PKV_RESHAPE_FUSED_MIN_CTAS)
+    reshape_rows_fused_kernel(const __grid_constant__ ReshapeParams p)
+{
+    pkv::grid_dep_entry();  // before any global memory access
+    const RowCoords rc = row_coords(p);
+    const uint32_t bs = p.div_bs.d;
+    int32_t rq[kReshapeUnroll], ps[kReshapeUnroll];  // this pass's tokens' request and position
+#pragma unroll
+    for (int u = 0; u < kReshapeUnroll; u++) {
+        const uint32_t tk = rc.tok0 + u * p.tok_step;
+        rq[u] = tk < p.n_tokens ? p.token_req[tk] : -1;
+        ps[u] = tk < p.n_tokens ? p.token_pos[tk] : 0;
+    }
+    for (uint32_t tok = rc.tok0; tok < p.n_tokens; tok += p.tok_step * kReshapeUnroll) {
+        uint4 v[kReshapeUnroll];
+        int32_t blk[kReshapeUnroll];  // table entry, or -1: the token has no slot
+        uint32_t off[kReshapeUnroll];
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            const uint32_t tk = tok + u * p.tok_step;
+            if (tk < p.n_tokens) v[u] = pkv::ld_once(rc.src + (int64_t)tk * p.src_token_stride);
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            blk[u] = -1;
+            off[u] = 0;
+            if (rq[u] >= 0 && rq[u] < p.n_reqs && ps[u] >= 0) {
+                const uint32_t q = pkv::fdiv((uint32_t)ps[u], p.div_bs);
+                if (q < (uint32_t)p.max_blocks) {
+                    blk[u] = p.table[(int64_t)rq[u] * p.table_row_stride + q];
+                    off[u] = (uint32_t)ps[u] - q * bs;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {  // the next pass's requests and positions
+            const uint32_t tk = tok + (kReshapeUnroll + u) * p.tok_step;
+            rq[u] = tk < p.n_tokens ? p.token_req[tk] : -1;
+            ps[u] = tk < p.n_tokens ? p.token_pos[tk] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kReshapeUnroll; u++) {
+            const uint32_t tk = tok + u * p.tok_step;
+            if (tk >= p.n_tokens) continue;
+            if (rc.reporter && p.slot_out != nullptr) p.slot_out[tk] = blk[u] < 0 ? -1 : (int64_t)blk[u] * bs + off[u];
+            if (blk[u] < 0) {
+                if (rc.reporter) pkv::set_error(p.err, KV_DERR_TABLE);
+                continue;
+            }
+            if ((int64_t)blk[u] * bs + off[u] >= (int64_t)p.slot_limit) {
+                pkv::set_error(p.err, KV_DERR_SLOT);
+                continue;
+            }
+            pkv::st_stream(rc.dst + (int64_t)blk[u] * p.block_stride + (int64_t)off[u] * p.token_stride, v[u]);
         }
     }
 }
@@ -260,6 +321,15 @@ int validate_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t ne
 
 constexpr int kRowThreads = 256;
 constexpr int64_t kMaxRowGroup = 16;
+
+// CTAs a grid stride must be a multiple of to cover whole tokens (planes x chunks per row
+// divides 256 x CTAs), or 0 when that is above kMaxRowGroup and the general kernel runs.
+int64_t row_group_ctas(const kv_cache_desc *cache)
+{
+    const int64_t per_token = cache->n_planes * (int64_t)(cache->row_bytes / 16);
+    const int64_t g = per_token / std::gcd<int64_t>(kRowThreads, per_token);
+    return PKV_RESHAPE_ROWS && g <= kMaxRowGroup ? g : 0;
+}
 
 // CTAs per tensor of a row-write launch: enough for the work, at most about four waves of
 // 8 resident CTAs per SM over the nt tensors of the launch.
@@ -298,26 +368,24 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
     p.n_planes = cache->n_planes;
     p.n_tokens = (uint32_t)n_tokens;
     p.err = dev->err_word;
-    // CTAs a grid stride must be a multiple of to cover whole tokens (planes x chunks per row
-    // divides 256 x CTAs); above kMaxRowGroup the general kernel runs instead.
-    const int64_t row_group = cache->n_planes * cpr / std::gcd<int64_t>(kRowThreads, cache->n_planes * cpr);
+    const int64_t row_group = row_group_ctas(cache);
 
-    int64_t *slot_out = p.slot_out;
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
         const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
+        if (t0 > 0) p.slot_out = nullptr;  // every launch covers the same tokens
         for (int32_t t = 0; t < nt; t++) {
             p.dst[t] = cache->base[t0 + t];
             for (int32_t pl = 0; pl < cache->n_planes; pl++)
                 p.src[t * cache->n_planes + pl] = new_kv[(int64_t)(t0 + t) * cache->n_planes + pl];
         }
-        p.slot_out = t0 == 0 ? slot_out : nullptr;
         int64_t per_tensor_ctas, cap;
         row_grid(cache, n_tokens, nt, *dev, &per_tensor_ctas, &cap);
         int64_t ctas = std::min(per_tensor_ctas, cap);
-        if (PKV_RESHAPE_ROWS && row_group <= kMaxRowGroup) {
+        if (row_group > 0) {
             ctas = (ctas + row_group - 1) / row_group * row_group;
             p.tok_step = (uint32_t)(ctas * kRowThreads / (cache->n_planes * cpr));
-            pkv::launch(reshape_rows_kernel<FUSED>, dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream, p);
+            pkv::launch(FUSED ? reshape_rows_fused_kernel : reshape_rows_kernel, dim3((unsigned)ctas, (unsigned)nt),
+                        kRowThreads, 0, stream, p);
         } else {
             pkv::launch(reshape_and_cache_kernel<FUSED>, dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream, p);
         }
@@ -332,7 +400,7 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
 int pkv::preload_write_kernels()
 {
     return pkv::load_kernels(slot_mapping_kernel, reshape_and_cache_kernel<true>, reshape_and_cache_kernel<false>,
-                             reshape_rows_kernel<true>, reshape_rows_kernel<false>);
+                             reshape_rows_kernel, reshape_rows_fused_kernel);
 }
 
 extern "C" {
@@ -377,24 +445,17 @@ int kv_write_tokens(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t 
                          (n_reqs > 0 && max_blocks_per_req > 0 && block_table == nullptr)))
         return KV_ERR_INVALID_ARG;
     if (n_reqs > 0 && bt_row_stride < max_blocks_per_req) return KV_ERR_INVALID_ARG;
-    // In the fused kernel every pass of a thread waits on the table lookup's two dependent
-    // loads.  With slot_out given, the batch runs as slot_mapping into slot_out followed by the
-    // plain row copy instead: the same results, and the row copy's launch overlaps slot_mapping
-    // (programmatic dependent launch), so it is faster for a decode write too.
+    // The row copy looks each token's slot up in the block table (and reports it in slot_out).
+    // A row shape that takes the general kernel, whose lookup is not pipelined, runs as
+    // slot_mapping followed by the plain row copy when slot_out can hold the slots.
     bool nothing = false;
     int st = validate_rows(cache, new_kv, new_token_stride, n_tokens, &nothing);
     if (st != KV_OK || nothing) return st;
-    if (slot_out != nullptr) {
-        const pkv::DeviceInfo *dev = pkv::current_device();
-        if (dev == nullptr) return KV_ERR_CUDA;
-        int64_t need, cap;
-        row_grid(cache, n_tokens, std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors), *dev, &need, &cap);
-        if (need > kWriteSplitIterations * cap) {
-            st = kv_slot_mapping(block_table, n_reqs, max_blocks_per_req, bt_row_stride, token_req, token_pos,
-                                 n_tokens, cache->block_size, slot_out, stream);
-            if (st != KV_OK) return st;
-            return kv_reshape_and_cache(cache, new_kv, new_token_stride, slot_out, n_tokens, stream);
-        }
+    if (slot_out != nullptr && row_group_ctas(cache) == 0) {
+        st = kv_slot_mapping(block_table, n_reqs, max_blocks_per_req, bt_row_stride, token_req, token_pos, n_tokens,
+                             cache->block_size, slot_out, stream);
+        if (st != KV_OK) return st;
+        return kv_reshape_and_cache(cache, new_kv, new_token_stride, slot_out, n_tokens, stream);
     }
     ReshapeParams p{};
     p.table = block_table;

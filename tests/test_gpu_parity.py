@@ -357,10 +357,13 @@ def test_empty_remap_step():
     G.compare(gpu, ora, "empty remap step")
 
 
+@pytest.mark.parametrize("write", ["reshape", "write_tokens"])
 @pytest.mark.parametrize("layout", ["separate", "blocks_first"])
-def test_more_tensors_than_one_launch_carries(layout):
-    """130 and 257 cache tensors: reshape_and_cache, pack and unpack split into several launches
-    (128 tensor bases per launch); the staging offsets of later launches must continue."""
+def test_more_tensors_than_one_launch_carries(layout, write):
+    """130 and 257 cache tensors: the token write, pack and unpack split into several launches
+    (128 tensor bases per launch); the staging offsets of later launches must continue.  The
+    token write is kv_reshape_and_cache, or kv_write_tokens through an identity block table
+    (slot = position), whose slot_out must come back whole from the first launch alone."""
     for n_tensors in (130, 257):
         g = W.CacheGeom(layout, 24, 4, 1, 16)  # 32-byte rows, tiny tensors
         rng = np.random.default_rng(n_tensors)
@@ -376,7 +379,15 @@ def test_more_tensors_than_one_launch_carries(layout):
         scache = K.PagedCache.from_tensors(s_dev, layout)
         dcache = K.PagedCache.from_tensors(d_dev, layout)
         n_dev = [torch.from_numpy(x).cuda().view(torch.bfloat16).reshape(T, 1, 16) for x in new]
-        K.kv_reshape_and_cache(scache, n_dev, torch.from_numpy(slot).cuda())
+        if write == "reshape":
+            K.kv_reshape_and_cache(scache, n_dev, torch.from_numpy(slot).cuda())
+        else:
+            table = torch.arange(24, dtype=torch.int32, device="cuda").reshape(1, 24)
+            out = torch.full((T,), -7, dtype=torch.int64, device="cuda")
+            K.kv_write_tokens(scache, n_dev, table, torch.zeros(T, dtype=torch.int32, device="cuda"),
+                              torch.from_numpy(slot.astype(np.int32)).cuda(), out)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(out.cpu().numpy(), slot)
         t = lambda a: torch.from_numpy(a).cuda()
         x = K.kv_build_xfer_list(t(off), t(ids), t(dids), 2)
         stage = K.kv_pack_blocks(scache, x, ids.shape[0])
