@@ -1,4 +1,5 @@
-// kv_slot_mapping and kv_reshape_and_cache: writing new tokens' K/V into the paged cache.
+// kv_slot_mapping, kv_reshape_and_cache and kv_write_tokens: writing new tokens' K/V into the
+// paged cache.
 //
 // Slot formula: drawing "vllm v1 调度逻辑 和 distributed 分布式原理", label "batch tensor 组装";
 // block = slots 0..15 of K/V rows: label "Paged kv cache"; one block_table serves every
