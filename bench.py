@@ -13,6 +13,12 @@ in GB/s, summed over ranks.  Inputs are larger than L2 (the step moves ~11 GB).
 Under torchrun each rank runs an independent replica on its own GPU (weak scaling).
 --impl reference times the CPU oracle (the plain C statement of the same step) on the
 host cores on a bounded sample of the same workload.
+
+Other modes: --stage host (staging in pinned host memory), --sw-window N (the
+sliding-window clip before the builder), --layers / --num-blocks (reduced cases for
+profiling captures), and two profiling drivers that print one JSON line of their own:
+--write-only (the new-token write alone: the two calls and kv_write_tokens) and
+--hash-only (kv_block_hashes alone).
 """
 from __future__ import annotations
 
