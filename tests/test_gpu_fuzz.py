@@ -23,6 +23,7 @@ import oracle
 from paged_kv_cache_81_gb300 import pagedkv as K
 from paged_kv_cache_81_gb300 import workloads as W
 from tests import gpu_support as G
+from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
 
@@ -186,3 +187,59 @@ def test_fuzz_hashes_match_oracle(seed):
         np.testing.assert_array_equal(o.cpu().numpy(), want_o)
         np.testing.assert_array_equal(h[:int(want_o[-1])].cpu().numpy().view(np.uint64), want, err_msg=f"ws {ws}")
     assert K.kv_get_last_error() == 0
+
+
+def fuzz_write_case(seed: int):
+    """A random token write: geometry (any layout, block sizes 1-32, 1-4 heads of 8-200 elements,
+    so rows of 1 to 50 chunks and both row kernels), 1-3 layers, a block table with holes, tokens
+    at distinct slots plus a few invalid ones, and the batch size (one token to several passes)."""
+    rng = np.random.default_rng(30_000 + seed)
+    layout = str(rng.choice(["separate", "blocks_first", "kv_first", "mla"]))
+    bs = int(rng.choice([1, 2, 3, 8, 16, 32]))
+    hd = int(rng.choice([8, 16, 24, 64, 72, 128, 136, 200]))
+    heads = 1 if layout == "mla" else int(rng.integers(1, 5))
+    n_reqs, width = int(rng.integers(1, 6)), int(rng.integers(1, 9))
+    nb = n_reqs * width + int(rng.integers(1, 16))
+    g = W.CacheGeom(layout, nb, bs, 1, heads * hd) if layout == "mla" else W.CacheGeom(layout, nb, bs, heads, hd)
+    table = rng.permutation(nb)[:n_reqs * width].astype(np.int32).reshape(n_reqs, width)
+    table[rng.random(table.shape) < 0.1] = -1  # holes
+    # distinct (request, position) pairs, so distinct slots; some invalid requests or positions
+    pairs = [(r, p) for r in range(n_reqs) for p in range(width * bs)]
+    T = int(rng.integers(1, min(len(pairs), int(rng.choice([8, 64, 4000]))) + 1))
+    pick = rng.choice(len(pairs), size=T, replace=False)
+    req = np.array([pairs[i][0] for i in pick], dtype=np.int32)
+    pos = np.array([pairs[i][1] for i in pick], dtype=np.int32)
+    bad = rng.random(T) < 0.05
+    req[bad & (rng.random(T) < 0.5)] = n_reqs
+    pos[bad & (req < n_reqs)] = width * bs + int(rng.integers(0, 3))
+    return rng, g, int(rng.integers(1, 4)), table, req, pos, bool(rng.integers(0, 2))
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_fuzz_write_tokens_match_oracle(seed):
+    """kv_write_tokens on random geometries and batches == the oracle's slot_mapping +
+    reshape_and_cache: every cache tensor, slot_out when given, and the error bits."""
+    rng, g, layers, table, req, pos, with_slot_out = fuzz_write_case(seed)
+    T = req.shape[0]
+    nt = layers * g.tensors_per_layer
+    src = W.host_cache_tensors(g, nt, rng)
+    new = [W.normal_bf16_bytes(rng, T * g.row_bytes // 2).reshape(T, g.row_bytes // 2) for _ in range(nt * g.n_planes)]
+    s_dev = W.to_device_bf16(src, "cuda")
+    n_dev = [x.reshape(G._new_shape(g, T)) for x in W.to_device_bf16(new, "cuda")]
+    cache = K.PagedCache.from_tensors(s_dev, g.layout)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.full((T,), -7, dtype=torch.int64, device="cuda") if with_slot_out else None
+    K.kv_get_last_error(clear=True)
+    K.kv_write_tokens(cache, n_dev, t(table), t(req), t(pos), out)
+    torch.cuda.synchronize()
+    err = K.kv_get_last_error(clear=True)
+    want_slot, n_bad = oracle.slot_mapping(table, req, pos, g.block_size)
+    assert ((err & K.KV_DERR_TABLE) != 0) == (n_bad > 0), f"error word {err:#x}, {n_bad} invalid tokens"
+    assert (err & ~K.KV_DERR_TABLE) == 0, f"error word {err:#x}"
+    if out is not None:
+        np.testing.assert_array_equal(out.cpu().numpy(), want_slot)
+    sc = H.ora_cache(g, [a.copy() for a in src])
+    assert oracle.reshape_and_cache(sc, [r.view(np.uint8) for r in new], want_slot) == 0
+    what = f"seed {seed}: {g.layout} bs {g.block_size} row {g.row_bytes} planes {g.n_planes} T {T} tensors {nt}"
+    for a, b in zip(s_dev, sc.tensors):
+        np.testing.assert_array_equal(a.cpu().view(torch.int16).numpy().view(np.uint16), b, err_msg=what)
