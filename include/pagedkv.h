@@ -23,6 +23,9 @@
  *  - Kernels are launched with programmatic stream serialisation allowed, so their CTAs may
  *    be scheduled while the previous kernel on `stream` still runs; each waits for that
  *    kernel to complete before its first memory access, so the data sees plain stream order.
+ *  - The first call of an entry point on a device sets up per-device state (launch
+ *    attributes, occupancy, symbol addresses; the first kv_wait_signal loads every kernel):
+ *    make it outside a stream capture.  Calls after it can be captured into CUDA graphs.
  *  - Payload bytes are opaque: rows are moved as 16-byte vectors and never converted,
  *    so NaN payloads, infinities and -0 arrive bit-exact.
  *  - Argument errors the host can see are returned at once and nothing is launched.
@@ -372,8 +375,9 @@ KV_API int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_o
  * While it polls, the work that sets the counter runs on another stream, and its kernels must
  * already be loaded: CUDA loads a kernel's code lazily, on first use, and that load may
  * synchronise the context, which would hold the producer's launch until this wait ends.  The
- * first call on a device loads every kernel of this library before it queues the poll; load
- * your own producer kernels first (run them once, or set CUDA_MODULE_LOADING=EAGER).  The
+ * first call on a device (outside a stream capture) loads every kernel of this library
+ * before it queues the poll; load your own producer kernels first (run them once, or set
+ * CUDA_MODULE_LOADING=EAGER).  The
  * kernels queued after the wait on `stream` are scheduled only once it ends, so they cannot
  * take the SM space the producer needs.
  */
