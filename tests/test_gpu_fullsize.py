@@ -9,7 +9,9 @@ cap and copy engine, as in the benchmark).  Then:
   * every tensor is checked on the device against properties that hold at any size: the
     staging equals torch advanced indexing of the source (the pages' layer[block_ids]), the
     destination blocks equal the staged ones, and every block or slot the step must not touch
-    still holds its seeded fill (regenerated on the device).
+    still holds its seeded fill (regenerated on the device);
+  * then fresh rows go through kv_write_tokens (the fused call, with slot_out): its slots equal
+    the oracle's, and every tensor's rows at those slots equal the fresh rows.
 """
 from __future__ import annotations
 
@@ -178,5 +180,23 @@ def test_full_size(wl):
                 assert torch.equal(dr[db, 0, ds, o:o + sl], toks), f"tensor {t}: remapped tokens misplaced"
                 assert torch.equal(dr[:, 0][keep2], dbase[:, 0][keep2]), f"tensor {t}: untouched dst slots changed"
             del dbase
-    del step, src, dst, new, stage
+
+    # --- kv_write_tokens at full size: fresh rows through the fused call -----
+    if case.n_tokens:
+        del new
+        new2 = W.new_token_rows(g, wl.n_tensors, case.n_tokens, dev, seed=seed + 3)
+        out = torch.full((case.n_tokens,), -7, dtype=torch.int64, device=dev)
+        K.kv_write_tokens(step.src, new2, step.block_table, step.token_req, step.token_pos, out)
+        torch.cuda.synchronize()
+        assert K.kv_get_last_error(clear=True) == 0
+        np.testing.assert_array_equal(out.cpu().numpy(), slot)
+        for t in range(wl.n_tensors):
+            sr = rows_dev(src[t], g)
+            for p in range(g.n_planes):
+                nr = new2[t * g.n_planes + p].reshape(case.n_tokens, -1).view(torch.uint8)
+                assert torch.equal(sr[blk, p, off], nr), f"tensor {t} plane {p}: kv_write_tokens rows not at their slots"
+        del new2
+    else:
+        del new
+    del step, src, dst, stage
     torch.cuda.empty_cache()
