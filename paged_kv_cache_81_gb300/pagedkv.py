@@ -243,8 +243,8 @@ def kv_reshape_and_cache(cache: PagedCache, new_kv: Sequence[torch.Tensor], slot
 def kv_write_tokens(cache: PagedCache, new_kv: Sequence[torch.Tensor], block_table: torch.Tensor,
                     token_req: torch.Tensor, token_pos: torch.Tensor, slot_out: Optional[torch.Tensor] = None,
                     stream=None):
-    """kv_slot_mapping + kv_reshape_and_cache in one call (one launch, or two for a large batch given
-    slot_out); slot_out (int64 [T]) optionally gets the slots."""
+    """kv_slot_mapping + kv_reshape_and_cache in one call: the row copy looks each token's slot up in
+    the block table (one launch per 128 tensors); slot_out (int64 [T]) optionally gets the slots."""
     _i32(token_req, "token_req"), _i32(token_pos, "token_pos")
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
         raise ValueError("block_table must be a row-major int32 [n_reqs, max_blocks] CUDA tensor")
