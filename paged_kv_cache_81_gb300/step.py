@@ -95,8 +95,8 @@ class TransferStep:
         K.kv_reshape_and_cache(self.src, self.new_kv, self.slot, stream)
 
     def write_tokens_call(self, stream=None):
-        """The same write as write_tokens through the one call kv_write_tokens, slots kept (it runs
-        the two kernels, the second launch overlapping the first)."""
+        """The same write as write_tokens through the one call kv_write_tokens, slots kept (the row
+        copy looks the slots up and writes them to self.slot)."""
         if not self.n_tokens:
             return
         K.kv_write_tokens(self.src, self.new_kv, self.block_table, self.token_req, self.token_pos, self.slot,
