@@ -552,9 +552,8 @@ def measure_single_request(step, dev, blocks: int = 64, iters: int = 200):
 def measure_write_path(step, dev, iters: int = 200) -> dict:
     """Wall-clock cost of the new-token write issued call by call from Python and replayed from a
     CUDA graph, in three forms: kv_slot_mapping + kv_reshape_and_cache; kv_write_tokens with
-    slot_out (the same two kernels behind one call); kv_write_tokens without slot_out (the slot
-    lookup fused into the row copy, one launch).  Plus each form's device time per write issued
-    back to back from a graph."""
+    slot_out; kv_write_tokens without slot_out (both one fused launch that looks the slots up in
+    the row copy).  Plus each form's device time per write issued back to back from a graph."""
     import torch
 
     def timed(fn):
