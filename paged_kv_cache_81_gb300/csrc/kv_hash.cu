@@ -22,6 +22,9 @@
 
 #include "kv_common.cuh"
 
+#ifndef PKV_HASH_W128
+#define PKV_HASH_W128 1  // 0: the table kernel loads each byte's weight on its own
+#endif
 #ifndef PKV_HASH_PDL
 #define PKV_HASH_PDL 1  // 0: plain stream-ordered launches for every hash kernel
 #endif
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
 {
     pkv::grid_dep_entry();  // before any global memory access
     __shared__ uint32_t sh_tok[kTableChunk];
-    __shared__ SplitWeight sh_w[kTableChunkBytes];
+    __shared__ __align__(16) SplitWeight sh_w[kTableChunkBytes];
     const int64_t n_hash = min((int64_t)out_off[n_reqs], limit);
     const uint32_t c0 = threadIdx.x;
     const int32_t nb = 4 * bs;  // token bytes per block
@@ -276,13 +279,25 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
 #pragma unroll 2
             for (int q = 0; q < m; q++) {
                 const uint32_t v = sh_tok[q];
+#if PKV_HASH_W128
+                // a token's 4 weights are 32 contiguous bytes (w + 4q is 32-byte aligned: chunks
+                // start at a multiple of 4 weights): two 16-byte loads instead of four 8-byte ones
+                const uint4 w01 = *reinterpret_cast<const uint4 *>(w + 4 * q);
+                const uint4 w23 = *reinterpret_cast<const uint4 *>(w + 4 * q + 2);
+                const uint32_t wl[4] = {w01.x, w01.z, w23.x, w23.z}, wh[4] = {w01.y, w01.w, w23.y, w23.w};
+#endif
 #pragma unroll
                 for (int byte = 0; byte < 4; byte++) {
                     const uint32_t x = c ^ ((v >> (8 * byte)) & 0xffu);
                     const int32_t d = (int32_t)x - (int32_t)c;
+#if PKV_HASH_W128
+                    acc += (int64_t)d * (int32_t)wl[byte];
+                    acc_hi += (uint32_t)d * wh[byte];
+#else
                     const SplitWeight wk = w[4 * q + byte];
                     acc += (int64_t)d * wk.lo_s;
                     acc_hi += (uint32_t)d * wk.hi;
+#endif
                     c = x * 0x1b3u;
                 }
             }
