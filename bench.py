@@ -171,7 +171,7 @@ class ClockSampler:
         except Exception:
             pass
         finally:
-            if self.path:
+            if self.path and os.path.exists(self.path):
                 os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
