@@ -152,3 +152,21 @@ def test_hash_workspace_size(lib):
     assert lib.kv_block_hashes_workspace_bytes(16, 0, ctypes.byref(out)) == K.KV_ERR_INVALID_ARG
     assert lib.kv_block_hashes_workspace_bytes(-1, 16, ctypes.byref(out)) == K.KV_ERR_INVALID_ARG
     assert lib.kv_block_hashes_workspace_bytes(16, 16, None) == K.KV_ERR_INVALID_ARG
+
+
+def test_header_and_c_example_compile_as_c11():
+    """pagedkv.h is a C header: the plain C11 caller (tests/c/abi_example.c) compiles against it with
+    every warning an error.  The CUDA runtime header comes from the toolkit next to nvcc."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    cuda_include = os.path.join(os.path.dirname(os.path.dirname(build.nvcc())), "include")
+    if not os.path.exists(os.path.join(cuda_include, "cuda_runtime.h")):
+        pytest.skip("no CUDA runtime header")
+    example = os.path.join(os.path.dirname(__file__), "c", "abi_example.c")
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I" + build.INCLUDE,
+                        "-I" + cuda_include, example], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
