@@ -26,6 +26,10 @@
  *  - The first call of an entry point on a device sets up per-device state (launch
  *    attributes, occupancy, symbol addresses; the first kv_wait_signal loads every kernel):
  *    make it outside a stream capture.  Calls after it can be captured into CUDA graphs.
+ *  - That per-device state (the error word's address, the static builder scratch's address,
+ *    occupancy figures) is kept for the life of the process and is not looked up again: it does
+ *    not survive cudaDeviceReset or a reset of the device's primary context.  A process that
+ *    resets a device must not call this library on that device afterwards.
  *  - Payload bytes are opaque: rows are moved as 16-byte vectors and never converted,
  *    so NaN payloads, infinities and -0 arrive bit-exact.
  *  - Argument errors the host can see are returned at once and nothing is launched.
@@ -37,12 +41,12 @@
  *
  * Sources (the vLLM PD-disaggregation pages this library restates):
  *  [S] drawing "vllm v1 调度逻辑 和 distributed 分布式原理": "batch tensor 组装" (the slot
- *      formula), "Paged kv cache" (16 slots per block), "总的就是 all kv cache" (one
+ *      formula), "Paged kv cache" (16 slots per block), the per-layer tensor panel (one
  *      tensor per layer, one block_table for all layers) and the two layer shapes.
  *  [N] page "0. vllm 如何使用 nccl 传输 kv cache", sections 2.3 (transfer flow) and 2.4
  *      (extract_kv_from_layer / inject_kv_into_layer).
- *  [F] page "5. flagcx connector design & dev & test", section 1.2 (xfer_list "per layer
- *      x per contiguous group x per req").
+ *  [F] page "5. flagcx connector design & dev & test", section 1.2 (the xfer_list, flattened
+ *      over layers, contiguous groups and requests).
  *  [M] page "vLLM PD 分离 源码级机制", sections 4.1 (receiver metadata: base addresses,
  *      block lengths, local block ids) and 4.2 (_build_transfer_params, _send_blocks).
  */
@@ -161,7 +165,7 @@ KV_API int kv_slot_mapping(const int32_t *block_table, int32_t n_reqs, int32_t m
                     int64_t n_tokens, int32_t block_size, int64_t *slot_out, kv_stream_t stream);
 
 /*
- * kv_reshape_and_cache [S "Paged kv cache", M timeline "KV Cache 写入本地显存"]:
+ * kv_reshape_and_cache [S "Paged kv cache", M section 6 timeline (prefill writes the KV cache into local GPU memory)]:
  * for every cache tensor t, plane p and token i with slot[i] >= 0,
  *     row (t, slot[i] / block_size, p, slot[i] % block_size) <- new_kv[t * n_planes + p] + i * new_token_stride
  * All tensors of the descriptor (e.g. every layer of a decode step) are written by one
@@ -366,7 +370,7 @@ KV_API int kv_unpack_blocks_signal(const kv_cache_desc *dst, int32_t dst_slice_o
                                    kv_stream_t stream);
 
 /*
- * kv_wait_signal [F section 1.2, flagcxWaitSignal: "GPU 侧 poll signal_buffer >= expected"]:
+ * kv_wait_signal [F section 1.2, flagcxWaitSignal: the receiver polls the signal counter on the GPU until it reaches the expected value]:
  * queues on `stream` a one-thread kernel that polls signal->value (acquire loads) until it
  * is >= expected, so work queued after it on `stream` starts only then.  The wait is
  * bounded: after timeout_us microseconds (1 .. 60,000,000; otherwise KV_ERR_RANGE) it gives

@@ -14,14 +14,14 @@
  *      "batch tensor 组装"  slot_mapping[flat_token_i] =
  *          block_table[req_i, position_i // block_size] * block_size + position_i % block_size
  *      "Paged kv cache"      block B3 holds tokens t0..t15 in slots 0..15, K/V per slot
- *      "总的就是 all kv cache" one tensor per layer, blocks contiguous inside a layer,
- *                            one block_table read by every layer
+ *      per-layer panel       one tensor per layer (layer_0 .. layer_47), blocks contiguous
+ *                            inside a layer, one block_table read by every layer
  *      last two labels       layer shapes (num_blocks, 2, bs, H, D) and (2, num_blocks, bs, H, D)
  *  [N] page "0. vllm 如何使用 nccl 传输 kv cache", section 2.4 (extract_kv_from_layer:
  *      layer[block_ids, ...] / layer[:, block_ids, ...]) and the transfer-flow step 14
  *      and consumer loop (kv_cache_layer[block_ids] = tensor)
  *  [F] page "5. flagcx connector design & dev & test", section 1.2: the sender flattens
- *      its work into an xfer_list "per layer x per contiguous group x per req"
+ *      its work into an xfer_list over layers, contiguous groups and requests
  *  [M] page "vLLM PD 分离 源码级机制", section 4.2: per-layer, per-block source and
  *      destination addresses; _send_blocks issues (src_ptrs, dst_ptrs, lengths)
  *

@@ -2,14 +2,14 @@
 // (page "5. flagcx connector design & dev & test", section 1.2): the sender adds 1 to a
 // per-pair signal counter with its last put of a transfer (sig_val = 1 on the last xfer),
 // and the receiver waits, on the GPU, until the counter reaches the largest value it
-// expects ("GPU 侧 poll signal_buffer >= expected") before its forward pass goes on.
+// expects (a GPU-side poll of the signal buffer) before its forward pass goes on.
 // Here kv_unpack_blocks_signal posts the increment when the last row of a scatter has
 // landed, and kv_wait_signal is the bounded device-side wait.
 #include "kv_common.cuh"
 
 namespace {
 
-constexpr uint64_t kMaxTimeoutUs = 60ull * 1000 * 1000;  // the pages' longest wait: ready.wait(60)
+constexpr uint64_t kMaxTimeoutUs = 60ull * 1000 * 1000;  // the pages' longest wait, 60 s (the proxy's ready event)
 
 __device__ __forceinline__ unsigned long long now_ns()
 {

@@ -3,7 +3,7 @@
 //
 // Slot formula: drawing "vllm v1 调度逻辑 和 distributed 分布式原理", label "batch tensor 组装";
 // block = slots 0..15 of K/V rows: label "Paged kv cache"; one block_table serves every
-// layer: label "总的就是 all kv cache".
+// layer: the per-layer tensor panel (layer_0 .. layer_47).
 #include <algorithm>
 #include <climits>
 #include <numeric>

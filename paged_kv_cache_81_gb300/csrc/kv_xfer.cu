@@ -1,6 +1,6 @@
 // kv_build_xfer_list: flattening per-request block lists into maximal contiguous runs.
 //
-// The sender's xfer_list "per layer x per contiguous group x per req" (page "5. flagcx
+// The sender's xfer_list, flattened over layers, contiguous groups and requests (page "5. flagcx
 // connector design & dev & test", section 1.2) needs, per request, the runs of
 // consecutive block ids; each run is one (source, destination, length) triple (page
 // "vLLM PD 分离 源码级机制", section 4.2, _send_blocks).  The layer factor is applied by

@@ -8,7 +8,7 @@ the CPU oracle all take its arrays as plain inputs.
 
 Sources for the shapes (vLLM PD-disaggregation pages):
   * "vllm v1 调度逻辑 和 distributed 分布式原理" drawing, "Paged kv cache": a block
-    holds token slots 0..15 (block_size 16); "总的就是 all kv cache": 48 layer
+    holds token slots 0..15 (block_size 16); the per-layer tensor panel: 48 layer
     tensors of 147456 blocks, 1.125 GB each, one block_table shared by every
     layer; "scheduler(step)": 8 prompts of "8k" take 576 x 8 blocks; the two
     layer shapes (num_blocks, 2, bs, H, D) and (2, num_blocks, bs, H, D).

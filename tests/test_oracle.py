@@ -376,7 +376,7 @@ def test_unpack_rejects_bad_lists():
 
 
 def test_page_layout_sizes():
-    """Drawing "总的就是 all kv cache": 48 layer tensors of 147456 blocks, 1.125 GB each;
+    """Drawing, per-layer tensor panel: 48 layer tensors of 147456 blocks, 1.125 GB each;
     "Paged kv cache": 16 slots per block; "scheduler(step)": 8 prompts -> 576 x 8 blocks."""
     g = W.PAGE.src
     assert g.tensor_shape() == (147456, 2, 16, 1, 128)
