@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import datetime
+import gc
 import hashlib
 import json
 import os
@@ -48,6 +49,13 @@ PG_TIMEOUT_S = 300  # process-group timeout under torchrun
 KERNEL_NAMES = ("slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack")
 COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_copy.cuh",
                 "paged_kv_cache_81_gb300/csrc/kv_bulk.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
+WRITE_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_write.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
+# the sources whose change makes a kernel's DRAM-traffic record stale
+KERNEL_SOURCES = {"pack": COPY_SOURCES, "unpack": COPY_SOURCES, "reshape_and_cache": WRITE_SOURCES}
+COPY_KERNELS = ("reshape_and_cache", "pack", "unpack")  # the bandwidth-bound kernels of a step
+# the other presets, measured at full size after the headline step (one after another)
+EXTRA_WORKLOADS = ("tiny", "mid", "mla", "asym_remap", "page_shaped_kv_first")
+EXTRA_TIMED_S = 0.5  # each extra workload's timed region lasts about this long
 
 
 def parse():
@@ -61,6 +69,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the context measurements after the timed steps (write path, prior art, prefix hash)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other presets' full-size runs after the headline step")
+    ap.add_argument("--workloads", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated presets measured at full size after the headline step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     ap.add_argument("--stage", default="device", choices=["device", "host"],
                     help="staging buffer in HBM, or in pinned host memory (pack/unpack over the host link)")
@@ -110,19 +122,21 @@ def source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes (read + write) per pack launch from the committed ncu summary of this workload,
-    or None when the summary is missing or the copy kernels' source changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"{workload}_pack_dram.md")
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per full-size launch of `kernel` from the committed ncu record of
+    this workload (profiles/<workload>_dram.json), or None when the record is missing, holds no
+    entry for the kernel, or the kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"{workload}_dram.json")
     try:
         with open(path) as f:
-            text = f.read()
-    except OSError:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("source_hash:", "pack_dram_bytes_per_launch:")))
-    if fields.get("source_hash", "").strip() != source_hash(COPY_SOURCES):
+    entry = rec.get("kernels", {}).get(kernel)
+    sources = KERNEL_SOURCES.get(kernel)
+    if not entry or not sources or entry.get("source_hash") != source_hash(sources):
         return None
-    return int(fields["pack_dram_bytes_per_launch"].strip())
+    return int(entry["bytes_per_launch_full"])
 
 
 class ClockSampler:
@@ -242,16 +256,11 @@ def run_ours(args):
     from paged_kv_cache_81_gb300 import build
     build.build()
     from paged_kv_cache_81_gb300 import pagedkv as K
-    from paged_kv_cache_81_gb300.step import TransferStep
 
     wl = workload(args)
     case = W.make_case(wl)
     seed = wl.seed * 7919 + rank
-    src = W.device_cache(wl.src, wl.n_tensors, dev, seed=seed)
-    dst = W.device_cache(wl.dst, wl.n_tensors, dev, seed=seed + 1) if wl.kind != "mla" else None
-    new = W.new_token_rows(wl.src, wl.n_tensors, case.n_tokens, dev, seed=seed + 2)
-    step = TransferStep(wl, case, src, dst, new, device=dev, host_stage=args.stage == "host",
-                        sw_window=args.sw_window or None)
+    step = make_step(wl, case, dev, seed, host_stage=args.stage == "host", sw_window=args.sw_window or None)
     stream = torch.cuda.current_stream(dev)
     K.kv_get_last_error(clear=True)
 
@@ -259,107 +268,15 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def slot_mapping():
-        if step.n_tokens:
-            K.kv_slot_mapping(step.block_table, step.token_req, step.token_pos, step.src.block_size, step.slot)
-
-    def reshape_and_cache():
-        if step.n_tokens:
-            K.kv_reshape_and_cache(step.src, step.new_kv, step.slot)
-
-    # the five calls of step.run(), split so that each is bracketed by its own events: the builder
-    # on the step's second stream (issued first, beside slot_mapping and reshape_and_cache), the
-    # rest on `stream`
-    side = step.side_stream()
-
-    def timed_step(e):
-        """One step.run(), bracketed: e[0] start, e[1] slot, e[2] reshape, e[3] joined, e[4] pack,
-        e[5] unpack on `stream`; e[6], e[7] around the builder on the side stream."""
-        e[0].record(stream)
-        side.wait_stream(stream)
-        e[6].record(side)
-        step.build(side)
-        e[7].record(side)
-        slot_mapping()
-        e[1].record(stream)
-        reshape_and_cache()
-        e[2].record(stream)
-        stream.wait_stream(side)
-        e[3].record(stream)
-        step.pack(stream)
-        e[4].record(stream)
-        step.unpack(stream)
-        e[5].record(stream)
-
-    brackets = {"slot_mapping": (0, 1), "reshape_and_cache": (1, 2), "build_xfer_list": (6, 7), "pack": (3, 4),
-                "unpack": (4, 5)}
-
-    for _ in range(max(3, args.warmup)):
-        step.run()
-    torch.cuda.synchronize(dev)
-    err = K.kv_get_last_error(clear=True)
-    if err:
-        raise RuntimeError(f"device error word {err:#x} after warm-up")
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    flush = step.bytes().total < FLUSH_BELOW_BYTES
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    start.record(stream)
-    for s in range(args.steps):
-        if flush:
-            flush_buf.fill_(s & 0xFF)  # evicts the previous step's data from L2, outside the step's events
-        timed_step(ev[s])
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    t_wall1 = time.time()
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
-    if flush:  # the sum of the steps' own durations, without the flushes between them
-        elapsed_ms = sum(ev[s][0].elapsed_time(ev[s][5]) for s in range(args.steps))
-    else:
-        elapsed_ms = start.elapsed_time(end)
-    per_kernel_all = {name: [ev[s][a].elapsed_time(ev[s][b]) for s in range(args.steps)]
-                      for name, (a, b) in brackets.items()}
-    per_kernel_ms = {name: statistics.mean(v) for name, v in per_kernel_all.items()}
-    err = K.kv_get_last_error(clear=True)
-    if err:
-        raise RuntimeError(f"device error word {err:#x} in the timed region")
-
-    elapsed_ms = reduce_max(elapsed_ms, dev)
-
+    t = run_timed(step, dev, stream, args.steps, args.warmup, barrier=barrier, gpu_index=local)
+    elapsed_ms = reduce_max(t["elapsed_ms"], dev)
     b = step.bytes()
-    per_bytes = {"slot_mapping": b.slot_mapping, "reshape_and_cache": b.reshape_and_cache,
-                 "build_xfer_list": b.build_xfer_list, "pack": b.pack, "unpack": b.unpack}
-    step_bytes = b.total
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+    value = world * b.total * args.steps / (elapsed_ms * 1e-3) / 1e9
 
     peak, peak_kind = peaks()
-    # pack is the kernel the metric names first; on the page-shaped step pack, unpack and
-    # reshape_and_cache take nearly equal time, so a "largest time" choice would flip between runs
-    dominant = "pack"
-    achieved = per_bytes[dominant] / (per_kernel_ms[dominant] * 1e-3) / 1e9
-    traffic = ncu_traffic(wl.name) if dominant == "pack" else None
-    kernels = {}
-    for name in KERNEL_NAMES:
-        if per_bytes[name] == 0:
-            continue
-        ms = per_kernel_ms[name]
-        gbs = per_bytes[name] / (ms * 1e-3) / 1e9
-        kernels[name] = {"ms": round(ms, 4), "ms_median": round(statistics.median(per_kernel_all[name]), 4),
-                         "ms_best": round(min(per_kernel_all[name]), 4), "bytes": per_bytes[name],
-                         "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                         "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
-    if step.n_tokens:
-        kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
+    kernels, per_bytes, per_kernel_ms = kernel_stats(step, t["per_kernel_all"], peak)
+    roofline = roofline_entry(wl.name, per_bytes, per_kernel_ms, peak, peak_kind)
 
     extras = not args.no_extras
     write_path = measure_write_path(step, dev) if extras and step.n_tokens else None
@@ -389,17 +306,12 @@ def run_ours(args):
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u8", "data": f"synthetic (seeded random cache contents and block lists of the {wl.name} workload)",
         "config": config_dict(wl, case, step),
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
-                     "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
-                     if peak_kind == "measured" else "of fallback", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "algorithmic_bytes_per_launch": per_bytes[dominant]},
+        "roofline": roofline,
         "kernels": kernels,
         "schedule": "build_xfer_list on a second stream beside slot_mapping + reshape_and_cache; pack, then "
                     "unpack, after both",
         "gpu_launches": args.steps * step.launches_per_step,
-        "clocks": clocks,
+        "clocks": t["clocks"],
         "e2e": e2e,
     }
     if write_path is not None:
@@ -413,6 +325,16 @@ def run_ours(args):
     if host_link is not None:
         line["host_link"] = host_link
         line["config"]["stage"] = "pinned host memory"
+    if extras and world == 1 and not args.no_workloads:
+        # the other presets at full size, one after another: the headline step's buffers go first
+        del step
+        gc.collect()
+        torch.cuda.empty_cache()
+        names = [n for n in args.workloads.split(",") if n and n != wl.name]
+        unknown = [n for n in names if n not in W.PRESETS]
+        if unknown:
+            raise SystemExit(f"unknown workloads {unknown}")
+        line["workloads"] = measure_workloads(names, dev, stream, peak, peak_kind, local)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, case, args.cpu_seconds)
         if extras:
@@ -421,6 +343,177 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def make_step(wl: W.Workload, case: W.Case, dev, seed: int, **kw):
+    """The workload's caches (seeded random bits on the device), new token rows and TransferStep."""
+    from paged_kv_cache_81_gb300.step import TransferStep
+
+    src = W.device_cache(wl.src, wl.n_tensors, dev, seed=seed)
+    dst = W.device_cache(wl.dst, wl.n_tensors, dev, seed=seed + 1) if wl.kind != "mla" else None
+    new = W.new_token_rows(wl.src, wl.n_tensors, case.n_tokens, dev, seed=seed + 2)
+    return TransferStep(wl, case, src, dst, new, device=dev, **kw)
+
+
+def run_timed(step, dev, stream, steps: int, warmup: int, barrier=lambda: None, gpu_index: int = 0) -> dict:
+    """W untimed warm-up steps, then exactly K timed steps between CUDA events on `stream`, with a
+    synchronize (and the barrier) on both sides and nvidia-smi clocks sampled meanwhile.
+
+    Every call of a step is bracketed by its own events: the builder on the step's second stream
+    (issued first, beside slot_mapping and reshape_and_cache), the rest on `stream`.  A step that
+    moves less than FLUSH_BELOW_BYTES gets an L2-flushing write before it, outside its events, and
+    the elapsed time is then the sum of the steps' own brackets."""
+    import torch
+    from paged_kv_cache_81_gb300 import pagedkv as K
+
+    side = step.side_stream()
+
+    def slot_mapping():
+        if step.n_tokens:
+            K.kv_slot_mapping(step.block_table, step.token_req, step.token_pos, step.src.block_size, step.slot)
+
+    def reshape_and_cache():
+        if step.n_tokens:
+            K.kv_reshape_and_cache(step.src, step.new_kv, step.slot)
+
+    def timed_step(e):
+        """One step.run(), bracketed: e[0] start, e[1] slot, e[2] reshape, e[3] joined, e[4] pack,
+        e[5] unpack on `stream`; e[6], e[7] around the builder on the side stream."""
+        e[0].record(stream)
+        side.wait_stream(stream)
+        e[6].record(side)
+        step.build(side)
+        e[7].record(side)
+        slot_mapping()
+        e[1].record(stream)
+        reshape_and_cache()
+        e[2].record(stream)
+        stream.wait_stream(side)
+        e[3].record(stream)
+        step.pack(stream)
+        e[4].record(stream)
+        step.unpack(stream)
+        e[5].record(stream)
+
+    brackets = {"slot_mapping": (0, 1), "reshape_and_cache": (1, 2), "build_xfer_list": (6, 7), "pack": (3, 4),
+                "unpack": (4, 5)}
+
+    for _ in range(max(3, warmup)):
+        step.run()
+    torch.cuda.synchronize(dev)
+    err = K.kv_get_last_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after warm-up")
+
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    flush = step.bytes().total < FLUSH_BELOW_BYTES
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    start.record(stream)
+    for s in range(steps):
+        if flush:
+            flush_buf.fill_(s & 0xFF)  # evicts the previous step's data from L2, outside the step's events
+        timed_step(ev[s])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if flush:  # the sum of the steps' own durations, without the flushes between them
+        elapsed_ms = sum(ev[s][0].elapsed_time(ev[s][5]) for s in range(steps))
+    else:
+        elapsed_ms = start.elapsed_time(end)
+    per_kernel_all = {name: [ev[s][a].elapsed_time(ev[s][b]) for s in range(steps)]
+                      for name, (a, b) in brackets.items()}
+    err = K.kv_get_last_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} in the timed region")
+    return {"elapsed_ms": elapsed_ms, "per_kernel_all": per_kernel_all, "clocks": clocks}
+
+
+def kernel_stats(step, per_kernel_all: dict, peak: float):
+    """Per-call entries (mean, median and best of the timed steps; algorithmic bytes; GB/s and the
+    fractions of the measured and the nominal HBM bandwidth) of one timed run."""
+    b = step.bytes()
+    per_bytes = {"slot_mapping": b.slot_mapping, "reshape_and_cache": b.reshape_and_cache,
+                 "build_xfer_list": b.build_xfer_list, "pack": b.pack, "unpack": b.unpack}
+    per_kernel_ms = {name: statistics.mean(v) for name, v in per_kernel_all.items()}
+    kernels = {}
+    for name in KERNEL_NAMES:
+        if per_bytes[name] == 0:
+            continue
+        ms = per_kernel_ms[name]
+        gbs = per_bytes[name] / (ms * 1e-3) / 1e9
+        kernels[name] = {"ms": round(ms, 4), "ms_median": round(statistics.median(per_kernel_all[name]), 4),
+                         "ms_best": round(min(per_kernel_all[name]), 4), "bytes": per_bytes[name],
+                         "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                         "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
+    if step.n_tokens:
+        kernels["reshape_and_cache"]["tokens_per_s"] = round(step.n_tokens / (per_kernel_ms["reshape_and_cache"] * 1e-3), 1)
+    return kernels, per_bytes, per_kernel_ms
+
+
+def roofline_entry(workload: str, per_bytes: dict, per_kernel_ms: dict, peak: float, peak_kind: str) -> dict:
+    """The roofline of the step's bound kernel: of the bandwidth-bound calls (reshape_and_cache,
+    pack, unpack) the one with the largest mean duration in this run, which is also the one
+    furthest below the HBM peak when they move the same bytes."""
+    cands = [k for k in COPY_KERNELS if per_bytes.get(k)]
+    dominant = max(cands, key=lambda k: per_kernel_ms[k])
+    achieved = per_bytes[dominant] / (per_kernel_ms[dominant] * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+            if peak_kind == "measured" else "of fallback", "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(workload, dominant),
+            "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "algorithmic_bytes_per_launch": per_bytes[dominant],
+            "choice": "the slowest of reshape_and_cache, pack and unpack (largest mean duration)"}
+
+
+def measure_workloads(names, dev, stream, peak: float, peak_kind: str, gpu_index: int) -> dict:
+    """Every other preset at full size, one after another, each on freshly allocated caches that are
+    freed before the next: the whole step timed for about EXTRA_TIMED_S (at least 5 steps, after 3
+    warm-up steps), with per-call events and clocks as for the headline step."""
+    import torch
+
+    out = {}
+    for name in names:
+        wl = W.PRESETS[name]
+        case = W.make_case(wl)
+        step = make_step(wl, case, dev, wl.seed * 7919)
+        probe = run_timed(step, dev, stream, 3, 3, gpu_index=gpu_index)  # also sizes the timed run
+        per_step_ms = max(probe["elapsed_ms"] / 3, 1e-3)
+        steps = int(min(200, max(5, EXTRA_TIMED_S * 1e3 // per_step_ms)))
+        t = run_timed(step, dev, stream, steps, 0, gpu_index=gpu_index)
+        kernels, per_bytes, per_kernel_ms = kernel_stats(step, t["per_kernel_all"], peak)
+        entry = {"config": config_dict(wl, case, step), "steps": steps,
+                 "ms_per_step": round(t["elapsed_ms"] / steps, 4),
+                 "value": round(step.bytes().total * steps / (t["elapsed_ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+                 "roofline": roofline_entry(wl.name, per_bytes, per_kernel_ms, peak, peak_kind),
+                 "kernels": kernels, "clocks": t["clocks"],
+                 "device_time": "CUDA events around each call on the stream it runs on, every timed step"}
+        if wl.kind == "mla" and step.n_tokens:
+            # the decode write is launch-bound: besides its events inside the eager steps above,
+            # its device time per write issued back to back from a CUDA graph
+            back_to_back = measure_write_device({"two_calls": step.write_tokens, "write_tokens": step.write_tokens_call,
+                                                 "fused": step.write_tokens_fused}, dev)
+            entry["decode_write"] = {"tokens": step.n_tokens, "tensors": len(step.src.tensors),
+                                     "eager_us_slot_mapping": round(kernels["slot_mapping"]["ms"] * 1e3, 2),
+                                     "eager_us_reshape_and_cache": round(kernels["reshape_and_cache"]["ms"] * 1e3, 2),
+                                     "device_us_per_write_back_to_back": back_to_back,
+                                     "tokens_per_s_back_to_back": round(step.n_tokens / (back_to_back["write_tokens"]
+                                                                                         * 1e-6), 1)}
+        out[name] = entry
+        del step
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
 
 
 def measure_prior_art(step, dev, stream, reps: int = 5):

@@ -7,6 +7,15 @@
 // then shared memory -> global with cp.async.bulk (bulk-group completion).  The copy
 // itself is done by the SM's TMA unit; no register ever holds payload.
 //
+// Work split as in the warp engine (kv_copy.cu): the persistent CTAs (one per SM) walk the first
+// items - items / kTailDiv items with a pipe stride; tail CTAs queued behind them take the rest in
+// chunks of kTailItemsPerPipe items per pipe, each placed on whichever SM frees up first, so SMs
+// that copy more slowly than others do not hold up the end of the launch.  Whole runs of 32-72 KiB
+// are coarser items than the warp engine's, and a third left to the tail measured best here
+// (Mid pack / unpack and MLA pack, GB/s: an eighth 6535 / 6521 and 6785; a quarter 6580 / 6631
+// and 6970, with some launches as slow as with an eighth; a third 6923 / 6917 and 6968; a half
+// 6915 / 6908 and 6955).  Copies with fewer than kTailMinItemsPerPipe items per pipe have no tail.
+//
 // One issuing lane per warp ("pipe") owns a ring of kSlots shared-memory slots.  A pipe
 // keeps up to kSlots - 1 loads in flight: before it loads into a slot it stores the oldest
 // loaded slot, then waits until all but the newest store have finished reading shared
@@ -28,6 +37,12 @@
 #ifndef PKV_BULK_PIPES
 #define PKV_BULK_PIPES 8
 #endif
+#ifndef PKV_BULK_TAIL_ITEMS
+#define PKV_BULK_TAIL_ITEMS 2  // items per pipe of one tail CTA
+#endif
+#ifndef PKV_BULK_TAIL_DIV
+#define PKV_BULK_TAIL_DIV 3  // 1 / (the share of the items left to the tail CTAs); 0: no tail CTAs
+#endif
 
 namespace {
 
@@ -38,6 +53,10 @@ constexpr int kSlots = PKV_BULK_SLOTS;
 constexpr int kPipes = PKV_BULK_PIPES;  // warps (pipes) per CTA
 constexpr int kBatch = 32;             // run records fetched per warp round
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr int64_t kTailDiv = PKV_BULK_TAIL_DIV;
+constexpr int kTailItemsPerPipe = PKV_BULK_TAIL_ITEMS;
+constexpr int kMaxTailCtasPerResident = 8;  // more tail chunks than this are strided over
+constexpr int64_t kTailMinItemsPerPipe = 8;  // fewer items per pipe: no tail (latency-bound copies)
 static_assert(kStage % 16 == 0 && kSlots >= 3, "bulk engine shape");
 
 struct PipeState {  // per pipe, in shared memory after the slot data
@@ -193,27 +212,41 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
     }
     if (nr < 0) nr = 0;
     const int64_t items = nr * p.n_tensors;  // item = tensor * nr + run, tensor-major
-    const int64_t g = (int64_t)blockIdx.x * kPipes + w;
-    const int64_t P = (int64_t)gridDim.x * kPipes;
+    // This pipe's k-th item (increasing in k).  Persistent CTA b: g + k * P over [0, n_static),
+    // g = b * kPipes + w, P = resident * kPipes.  Tail CTA b (b >= resident): item w + (k %
+    // kTailItemsPerPipe) * kPipes of chunk (b - resident) + (k / kTailItemsPerPipe) * n_tail_ctas
+    // of [n_static, items).
+    const int64_t P = (int64_t)p.resident * kPipes;
+    const int64_t n_static = p.tail_div > 0 ? (items - items / p.tail_div) / P * P : items;
+    const bool tail = (int64_t)blockIdx.x >= p.resident;
+    const int64_t chunk = (int64_t)kPipes * kTailItemsPerPipe;
+    const int64_t n_tail_ctas = (int64_t)gridDim.x - p.resident;
+    const int64_t g = tail ? (int64_t)blockIdx.x - p.resident : (int64_t)blockIdx.x * kPipes + w;
+    const int64_t item_end = tail ? items : n_static;
+    auto item_of = [&](int64_t k) -> int64_t {
+        if (tail)
+            return n_static + ((k / kTailItemsPerPipe) * n_tail_ctas + g) * chunk + w + (k % kTailItemsPerPipe) * kPipes;
+        return g + k * P;
+    };
     const int64_t block_bytes = p.stage_block_bytes;
     const int64_t span_bytes = (int64_t)p.div_cps.d * 16;  // one (block, plane) span
 
     kv_xfer_run next{};
     {
-        const int64_t it = g + (int64_t)lane * P;
-        if (it < items) next = p.runs[it % nr];
+        const int64_t it = item_of(lane);
+        if (it < item_end) next = p.runs[it % nr];
     }
-    for (int64_t round = 0; g + round * kBatch * P < items; round++) {
+    for (int64_t round = 0; item_of(round * kBatch) < item_end; round++) {
         st->rec[lane] = next;
         __syncwarp();
         {
-            const int64_t it = g + ((round + 1) * kBatch + lane) * P;  // prefetch the next round
-            if (it < items) next = p.runs[it % nr];
+            const int64_t it = item_of((round + 1) * kBatch + lane);  // prefetch the next round
+            if (it < item_end) next = p.runs[it % nr];
         }
         if (lane == 0 && !pipe.failed) {
             for (int i = 0; i < kBatch; i++) {
-                const int64_t item = g + (round * kBatch + i) * P;
-                if (item >= items) break;
+                const int64_t item = item_of(round * kBatch + i);
+                if (item >= item_end) break;
                 const int32_t t = (int32_t)(item / nr);
                 const kv_xfer_run run = st->rec[i];
                 if (run.n_blocks <= 0) continue;
@@ -275,8 +308,9 @@ int preload_bulk_kernels()
                         bulk_copy_kernel<false, false>);
 }
 
-int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s)
+int launch_bulk_copy(const CopyParams &params, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s)
 {
+    CopyParams p = params;
     static std::mutex mu;
     static bool configured[64][2][2];
     static int per_sm[64][2][2];
@@ -294,7 +328,19 @@ int launch_bulk_copy(const CopyParams &p, int mode, bool pack, const DeviceInfo 
             configured[di][m][d] = true;
         }
     }
-    pkv::launch(fn, dev.num_sms * per_sm[di][m][d], kPipes * 32, kSmemBytes, s, p);
+    // persistent CTAs, plus enough tail CTAs for the largest tail the device-side run count allows
+    p.resident = dev.num_sms * per_sm[di][m][d];
+    int64_t tail_ctas = 0;
+    const int64_t items_max = std::min<int64_t>(p.run_capacity, p.n_stage_blocks) * p.n_tensors;
+    const int64_t quantum = (int64_t)kPipes * p.resident;
+    p.tail_div = 0;
+    if (kTailDiv > 0 && items_max >= kTailMinItemsPerPipe * quantum) {
+        const int64_t chunk = (int64_t)kPipes * kTailItemsPerPipe;
+        p.tail_div = (int32_t)kTailDiv;
+        tail_ctas = std::max<int64_t>(1, std::min<int64_t>((items_max / std::max<int64_t>(1, kTailDiv) + quantum + chunk - 1) / chunk,
+                                                           (int64_t)kMaxTailCtasPerResident * p.resident));
+    }
+    pkv::launch(fn, p.resident + (int)tail_ctas, kPipes * 32, kSmemBytes, s, p);
     return cuda_status(cudaGetLastError());
 }
 

@@ -8,9 +8,20 @@
 //
 // Work decomposition: an item is one piece (at most kPieceChunks 16-byte chunks) of one
 // (tensor, run).  Items are numbered piece-major, then tensor, then run, so consecutive warps
-// write adjacent staging ranges and no warp keeps drawing empty pieces; the grid is
-// persistent (resident CTAs on every SM) and walks the items with a warp stride.  Inside a
-// piece each lane keeps kUnroll 16-byte loads in flight before storing them.
+// write adjacent staging ranges and no warp keeps drawing empty pieces.  The grid has two parts:
+//  - `resident` persistent CTAs (every CTA the SMs hold at once) walk the first 7/8 of the
+//    items with a warp stride, so the warps in flight work on one dense window of items;
+//  - tail CTAs, queued behind them, take the last 1/8 in chunks of kTailItemsPerWarp items per
+//    warp; the block scheduler places each on whichever SM frees up first.
+// Some SMs scatter rows measurably slower than others (on GB300 four groups of about ten SMs
+// took ~10% longer over the same static share of an unpack), so a purely static split waits for
+// them; the tail lets the faster SMs finish the work instead.  An eighth for the tail and a
+// quarter measured the same on the page-shaped, kv-first and asymmetric presets; with no tail
+// and purely hardware-scheduled CTAs (each a contiguous range of items) unpack ran as fast but
+// pack of whole 8 KiB blocks lost 3%, its staging writes spread over many small ranges.  A copy
+// with fewer than kTailMinItemsPerWarp items per warp has no tail.  Inside a CTA the warps draw their
+// items from a shared-memory ticket, so a warp that is ahead takes the next item of its CTA.
+// Inside a piece each lane keeps kUnroll 16-byte loads in flight before storing them.
 //
 // Address modes of the cache side (the staging side is always linear):
 //   MERGED  a run is one contiguous span (dense blocks, block_stride == staged block bytes)
@@ -42,10 +53,23 @@ using pkv::REMAP;
 #ifndef PKV_ROWS_MIN_CTAS
 #define PKV_ROWS_MIN_CTAS 1  // the same hint for the ROWS and REMAP modes (more index arithmetic per chunk)
 #endif
+#ifndef PKV_COPY_TAIL_DIV
+#define PKV_COPY_TAIL_DIV 8  // 1 / (the share of the items left to the tail CTAs)
+#endif
+#ifndef PKV_COPY_TAIL_ITEMS
+#define PKV_COPY_TAIL_ITEMS 2  // items per warp of one tail CTA
+#endif
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = PKV_COPY_UNROLL;
 constexpr uint32_t kPieceChunks = 1024;  // 16 KiB
+constexpr int64_t kTailDiv = PKV_COPY_TAIL_DIV;  // the tail CTAs take items / kTailDiv of the items
+constexpr int kTailItemsPerWarp = PKV_COPY_TAIL_ITEMS;  // a tail CTA's chunk: kWarps * this many items
+constexpr int kMaxTailCtasPerResident = 8;       // more tail chunks than this are strided over
+// A copy of fewer than this many items per warp of the persistent part has no tail: its time is
+// launch and latency, and a second round of CTAs would only add to it.
+constexpr int64_t kTailMinItemsPerWarp = 8;
 
 template <int MODE, bool PACK>
 __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTAS : PKV_COPY_MIN_CTAS)
@@ -53,11 +77,13 @@ __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTA
 {
     pkv::grid_dep_entry();  // before any global memory access
     const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const unsigned wib = threadIdx.x >> 5;  // warp in the CTA
+    __shared__ unsigned s_ticket;           // the CTA's next item ticket
+    if (threadIdx.x == 0) s_ticket = kWarps;  // tickets 0 .. kWarps-1 are the warps' first items
+    __syncthreads();
     int64_t nr = *p.n_runs;
     if (nr > p.run_capacity) {
-        if (warp == 0 && lane == 0) pkv::set_error(p.err, KV_DERR_CAPACITY);
+        if (blockIdx.x == 0 && threadIdx.x == 0) pkv::set_error(p.err, KV_DERR_CAPACITY);
         nr = p.run_capacity;
     }
     if (nr < 0) nr = 0;
@@ -66,14 +92,35 @@ __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTA
     const int64_t per_piece = nr * p.n_tensors;
     const int64_t items = per_piece * p.max_pieces;
 
-    int64_t item = warp;
+    // Ticket i of this CTA -> item.  Persistent CTA b: round i / kWarps of the warp-stride walk
+    // over [0, n_static), slot b * kWarps + i % kWarps.  Tail CTA b (b >= resident): item i %
+    // chunk of chunk (b - resident) + (i / chunk) * n_tail_ctas of [n_static, items).  Both are
+    // increasing in i, so the first item past the end ends the warp's walk.
+    const int64_t quantum = (int64_t)kWarps * p.resident;
+    const int64_t n_static = p.tail_div > 0 ? (items - items / p.tail_div) / quantum * quantum : items;
+    const bool tail = (int64_t)blockIdx.x >= p.resident;
+    const int64_t chunk = (int64_t)kWarps * kTailItemsPerWarp;
+    const int64_t n_tail_ctas = (int64_t)gridDim.x - p.resident;
+    const int64_t slot = tail ? (int64_t)blockIdx.x - p.resident : (int64_t)blockIdx.x * kWarps;
+    const int64_t item_end = tail ? items : n_static;
+    auto item_of = [&](unsigned i) -> int64_t {
+        if (tail) return n_static + ((int64_t)(i / chunk) * n_tail_ctas + slot) * chunk + i % chunk;
+        return (int64_t)(i / kWarps) * quantum + slot + i % kWarps;
+    };
+    auto next_ticket = [&]() -> unsigned {
+        unsigned t = 0;
+        if (lane == 0) t = atomicAdd(&s_ticket, 1u);
+        return __shfl_sync(0xffffffffu, t, 0);
+    };
+
+    int64_t item = item_of(wib);
     kv_xfer_run next;
-    if (item < items) next = p.runs[item % per_piece % nr];
-    while (item < items) {
+    if (item < item_end) next = p.runs[item % per_piece % nr];
+    while (item < item_end) {
         const int64_t cur = item;
         const kv_xfer_run run = next;
-        item += n_warps;
-        if (item < items) next = p.runs[item % per_piece % nr];  // prefetch: overlaps the copy below
+        item = item_of(next_ticket());
+        if (item < item_end) next = p.runs[item % per_piece % nr];  // prefetch: overlaps the copy below
         const int32_t piece = (int32_t)(cur / per_piece);
         const int64_t rest = cur - (int64_t)piece * per_piece;
         const int32_t t = (int32_t)(rest / nr);
@@ -311,7 +358,20 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     const int64_t piece = mode == SPANS ? stage_block_bytes / stage->n_planes : stage_block_bytes;
     const bool bulk = !host_stage && (mode == MERGED || mode == SPANS) && bulk_engine(piece);
     const KernelFn fn = pick(mode, pack);
-    const int grid = bulk ? 0 : dev->num_sms * resident_ctas(dev->device, mode, pack);
+    int grid = 0;
+    if (!bulk) {
+        // persistent CTAs, plus enough tail CTAs for the largest tail the device-side run count
+        // allows (a tail CTA whose chunk lies past the items exits at once)
+        p.resident = dev->num_sms * resident_ctas(dev->device, mode, pack);
+        const int64_t items_max = (int64_t)std::min<int64_t>(run_capacity, stage->n_blocks) * p.max_pieces *
+                                  std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors);
+        const int64_t quantum = (int64_t)kWarps * p.resident;
+        const int64_t chunk = (int64_t)kWarps * kTailItemsPerWarp;
+        const bool with_tail = kTailDiv > 0 && items_max >= kTailMinItemsPerWarp * quantum;
+        p.tail_div = with_tail ? (int32_t)kTailDiv : 0;
+        const int64_t tail_ctas = (items_max / std::max<int64_t>(1, kTailDiv) + quantum + chunk - 1) / chunk;
+        grid = p.resident + (with_tail ? (int)std::max<int64_t>(1, std::min<int64_t>(tail_ctas, (int64_t)kMaxTailCtasPerResident * p.resident)) : 0);
+    }
     for (int32_t t0 = 0; t0 < cache->n_tensors; t0 += pkv::kMaxTensorsPerLaunch) {
         const int32_t nt = std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors - t0);
         p.n_tensors = nt;

@@ -29,6 +29,8 @@ struct CopyParams {
     int32_t n_tensors;
     int32_t tensor_begin;
     int32_t max_pieces;
+    int32_t resident;           // CTAs of the grid's persistent part
+    int32_t tail_div;           // the grid's tail CTAs take items / tail_div of the items (0: no tail)
     uint32_t chunks_per_block;  // staged block / 16
     FastDiv div_cpr;            // chunks per staged row
     FastDiv div_bs;             // staged (source) block size

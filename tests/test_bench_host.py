@@ -2,6 +2,7 @@
 and the parsing of the nvidia-smi clock samples taken during the timed region."""
 from __future__ import annotations
 
+import json
 import os
 import re
 
@@ -10,23 +11,47 @@ import bench
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _record():
-    with open(os.path.join(ROOT, "profiles", "page_shaped_pack_dram.md")) as f:
-        text = f.read()
-    h = re.search(r"^source_hash: (\w+)$", text, re.M).group(1)
-    b = int(re.search(r"^pack_dram_bytes_per_launch: (\d+)$", text, re.M).group(1))
-    return h, b
+def _write_record(root, kernels: dict):
+    os.makedirs(os.path.join(root, "profiles"), exist_ok=True)
+    with open(os.path.join(root, "profiles", "wl_dram.json"), "w") as f:
+        json.dump({"workload": "wl", "kernels": kernels}, f)
 
 
-def test_traffic_reported_only_for_the_sources_it_was_taken_on(monkeypatch):
-    h, b = _record()
-    # the record is plausible: DRAM bytes of one full-size pack launch, near its algorithmic bytes
-    assert 0.9 < b / 3_623_878_656 < 1.02
-    monkeypatch.setattr(bench, "source_hash", lambda paths: h)
-    assert bench.ncu_traffic("page_shaped") == b
-    monkeypatch.setattr(bench, "source_hash", lambda paths: "0" * 16)  # the copy kernels changed
-    assert bench.ncu_traffic("page_shaped") is None
-    assert bench.ncu_traffic("no_such_workload") is None
+def test_traffic_reported_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    hashes = {"pack": "a" * 16, "reshape_and_cache": "b" * 16}
+    monkeypatch.setattr(bench, "source_hash", lambda paths: hashes["pack" if paths == bench.COPY_SOURCES
+                                                                   else "reshape_and_cache"])
+    _write_record(str(tmp_path), {"pack": {"source_hash": "a" * 16, "bytes_per_launch_full": 123},
+                                  "unpack": {"source_hash": "0" * 16, "bytes_per_launch_full": 456},
+                                  "reshape_and_cache": {"source_hash": "b" * 16, "bytes_per_launch_full": 789}})
+    assert bench.ncu_traffic("wl", "pack") == 123
+    assert bench.ncu_traffic("wl", "unpack") is None  # taken on other copy sources
+    assert bench.ncu_traffic("wl", "reshape_and_cache") == 789
+    assert bench.ncu_traffic("wl", "slot_mapping") is None  # no record for this kernel
+    assert bench.ncu_traffic("no_such_workload", "pack") is None
+
+
+def test_committed_traffic_records_are_plausible():
+    """Every committed DRAM record holds, per kernel, the capture's bytes and the full-size
+    figure scaled from it by the stated factor, near the kernel's algorithmic bytes."""
+    algorithmic = {"page_shaped": {"pack": 3_623_878_656, "unpack": 3_623_878_656,
+                                   "reshape_and_cache": 3_624_468_480}}
+    for name in os.listdir(os.path.join(ROOT, "profiles")):
+        if not name.endswith("_dram.json"):
+            continue
+        with open(os.path.join(ROOT, "profiles", name)) as f:
+            rec = json.load(f)
+        scale = rec["scale"]
+        assert scale >= 1
+        for kernel, e in rec["kernels"].items():
+            assert kernel in bench.KERNEL_SOURCES
+            assert re.fullmatch(r"[0-9a-f]{16}", e["source_hash"])
+            per_launch = (e["dram_read_bytes"] + e["dram_write_bytes"]) / e["launches"]
+            assert abs(e["bytes_per_launch_full"] - round(per_launch * scale)) <= 1
+            want = algorithmic.get(rec["workload"], {}).get(kernel)
+            if want:
+                assert 0.9 < e["bytes_per_launch_full"] / want < 1.05, (name, kernel)
 
 
 def test_source_hash_follows_every_copy_source(tmp_path, monkeypatch):
