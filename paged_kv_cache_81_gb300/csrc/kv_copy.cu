@@ -261,10 +261,12 @@ int resident_ctas(int device, int mode, bool pack)
     return slot;
 }
 
-// Copy engine for whole contiguous blocks.  The TMA bulk-copy engine (kv_bulk.cu) moves
-// blocks of 16 KiB and more faster than the register-staged warp engine above; for smaller
-// blocks the two measure within noise of each other and the warp engine is kept.
-// PAGEDKV_COPY_ENGINE=lsu|bulk (read once) forces one engine for measurements.
+// Copy engine for contiguous spans (whole runs, or one span per (block, plane)).  With both
+// engines on the persistent-plus-tail work split, the TMA bulk-copy engine (kv_bulk.cu) moves
+// spans of 4 KiB and more faster than the register-staged warp engine above (GB/s, pack /
+// unpack, full presets: 8 KiB blocks 6836 / 6854 against 6564 / 6788; kv-first 4 KiB planes
+// 6823 / 6835 against 6737 / 6761; 32 KiB blocks 6933 / 6929).  Smaller spans keep the warp
+// engine.  PAGEDKV_COPY_ENGINE=lsu|bulk (read once) forces one engine for measurements.
 bool bulk_engine(int64_t block_bytes)
 {
     static const int forced = [] {
@@ -275,7 +277,7 @@ bool bulk_engine(int64_t block_bytes)
         return 0;
     }();
     if (forced) return forced == 1;
-    return block_bytes >= 16 * 1024;
+    return block_bytes >= 4 * 1024;
 }
 
 // The staging buffer may be device memory or pinned host memory (cudaHostAlloc /

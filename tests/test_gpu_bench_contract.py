@@ -16,7 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
 def test_bench_json_line():
     r = subprocess.run([sys.executable, "bench.py", "--workload", "tiny", "--steps", "5", "--warmup", "3",
-                        "--cpu-seconds", "0.5"], cwd=ROOT, capture_output=True, text=True, timeout=900)
+                        "--cpu-seconds", "0.5", "--workloads", "mla,asym_remap"], cwd=ROOT, capture_output=True,
+                       text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -40,6 +41,21 @@ def test_bench_json_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 5 * 5  # slot_mapping, reshape_and_cache, builder, pack, unpack per step
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    # the roofline describes the slowest of the bandwidth-bound calls
+    copies = {k: d["kernels"][k]["ms"] for k in ("reshape_and_cache", "pack", "unpack") if k in d["kernels"]}
+    assert rf["kernel"] == max(copies, key=copies.get)
+    # the other presets, each at full size with its own timed steps, clocks and roofline
+    w = d["workloads"]
+    assert set(w) == {"mla", "asym_remap"}
+    for name, e in w.items():
+        assert e["config"]["workload"] == name and e["steps"] >= 5 and e["value"] > 0
+        assert e["roofline"]["kernel"] in e["kernels"] and e["roofline"]["frac"] > 0
+        assert set(e["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    assert w["mla"]["config"]["layers"] == 61 and w["mla"]["config"]["num_blocks"] == 8192
+    assert set(w["mla"]["kernels"]) >= {"pack", "reshape_and_cache"} and "unpack" not in w["mla"]["kernels"]
+    assert w["mla"]["decode_write"]["tokens"] == 256
+    assert all(v > 0 for v in w["mla"]["decode_write"]["device_us_per_write_back_to_back"].values())
+    assert w["asym_remap"]["config"]["dst_block_size"] == 64 and "unpack" in w["asym_remap"]["kernels"]
 
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
@@ -47,7 +63,7 @@ def test_bench_json_line():
                                                                             "--num-blocks", "2048"]],
                          ids=["host_staging", "sliding_window", "mid_shrunk"])
 def test_bench_modes_print_one_line(flags):
-    args = [sys.executable, "bench.py", "--steps", "3", "--warmup", "3", "--no-cpu-baseline"]
+    args = [sys.executable, "bench.py", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-workloads"]
     if "--workload" not in flags:
         args += ["--workload", "tiny"]
     r = subprocess.run(args + flags, cwd=ROOT, capture_output=True, text=True, timeout=900)

@@ -176,15 +176,21 @@ def test_pack_layouts(layout, sl):
     assert K.kv_get_last_error() == 0
 
 
-@pytest.mark.parametrize("layout,heads", [("kv_first", 8), ("blocks_first", 4)],
-                         ids=["kv_first_16KiB_planes_spans", "blocks_first_16KiB_blocks_merged"])
-def test_tma_engine_layouts(layout, heads):
-    """Whole steps whose contiguous pieces reach 16 KiB, so pack and unpack take the TMA bulk
-    engine: kv-first planes of 16 KiB (SPANS: one bulk copy per plane of a block) and
-    blocks-first blocks of 16 KiB (MERGED), against the oracle."""
+@pytest.mark.parametrize("layout,heads,engine", [("kv_first", 1, "warp"), ("kv_first", 2, "tma"), ("kv_first", 8, "tma"),
+                                                 ("separate", 1, "warp"), ("blocks_first", 1, "tma"),
+                                                 ("blocks_first", 4, "tma")],
+                         ids=["kv_first_2KiB_planes_spans_warp", "kv_first_4KiB_planes_spans_tma",
+                              "kv_first_16KiB_planes_spans_tma", "separate_2KiB_blocks_merged_warp",
+                              "blocks_first_4KiB_blocks_merged_tma", "blocks_first_16KiB_blocks_merged_tma"])
+def test_copy_engine_layouts(layout, heads, engine):
+    """Whole steps on both copy engines, against the oracle.  Contiguous spans (a whole block, or
+    one plane of a kv-first block) of 4 KiB and more take the TMA bulk engine (SPANS: one bulk
+    copy per plane of a block; MERGED: one per run), smaller spans the register-staged warp
+    engine."""
     from dataclasses import replace
     g = W.CacheGeom(layout, 64, 16, heads, 64)
-    assert g.block_payload_bytes // (g.n_planes if layout == "kv_first" else 1) >= 16 * 1024
+    span = g.block_payload_bytes // (g.n_planes if layout == "kv_first" else 1)
+    assert (span >= 4 * 1024) == (engine == "tma")
     wl = replace(W.TINY, name=f"tma_{layout}", src=g, dst=g)
     case = W.make_case(wl)
     src, dst, new = G.host_inputs(wl, case, seed=wl.seed + 41)
@@ -312,11 +318,12 @@ def test_host_argument_errors():
     assert K.kv_get_last_error() == 0
 
 
-@pytest.mark.parametrize("heads", [4, 8], ids=["8KiB_blocks_warp_engine", "16KiB_blocks_tma_engine"])
+@pytest.mark.parametrize("heads", [1, 4, 8], ids=["2KiB_blocks_warp_engine", "8KiB_blocks_tma_engine",
+                                                   "16KiB_blocks_tma_engine"])
 def test_run_past_the_staging_buffer_flagged(heads):
     """Runs built for four blocks, pack and unpack told the staging buffer holds three: the run
     staged past the end is skipped and flagged (KV_DERR_STAGE); the other runs still move."""
-    g = W.CacheGeom("separate", 16, 16, heads, 64)  # heads * 128 B rows; 8 or 16 KiB blocks
+    g = W.CacheGeom("separate", 16, 16, heads, 64)  # heads * 128 B rows; 2, 8 or 16 KiB blocks
     rng = np.random.default_rng(31)
     src = W.to_device_bf16(W.host_cache_tensors(g, 1, rng), "cuda")
     dst = W.to_device_bf16(W.host_cache_tensors(g, 1, rng), "cuda")

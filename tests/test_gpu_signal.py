@@ -45,7 +45,7 @@ def _signalled_unpack(step: TransferStep, signal, add):
                            signal_add=add)
 
 
-# small page: register-staged engine; small mid: TMA bulk engine; small asym: token remap
+# small page and small mid: TMA bulk engine (8 and 32 KiB blocks); small asym: token remap (warp engine)
 @pytest.mark.parametrize("wl", [W.small(W.PAGE), W.small(W.MID), W.small(W.ASYM)], ids=lambda w: w.name)
 def test_unpack_signal_then_wait(wl):
     case = W.make_case(wl)
@@ -115,14 +115,15 @@ def test_wait_argument_checks():
     assert lib.kv_wait_signal(None, 1, 10, None, K._stream()) == K.KV_ERR_INVALID_ARG
 
 
-def test_wait_then_copy_leaves_room_for_the_producer():
+@pytest.mark.parametrize("row", [128, 256], ids=["2KiB_blocks_warp_engine", "4KiB_blocks_tma_engine"])
+def test_wait_then_copy_leaves_room_for_the_producer(row):
     """Stream A waits for a counter that a signalled unpack on stream B sets, then packs: a
     persistent grid that fills every SM.  The pack must not be scheduled while the wait polls, or
     it would hold the SM space the unpack needs and the wait would run out.  B starts late (a
     sleep kernel), so A's wait is already polling when the unpack is queued.  The pack reads the
     blocks the unpack wrote, ordered by the counter, and must return the staged bytes."""
-    n, bs, row = 40, 16, 256
-    g = W.CacheGeom("separate", 256, bs, 1, row // 2)  # 4 KiB blocks: the register-staged engine
+    n, bs = 40, 16
+    g = W.CacheGeom("separate", 256, bs, 1, row // 2)  # 2 KiB blocks: the warp engine; 4 KiB: the TMA engine
     rng = np.random.default_rng(31)
     cache = K.PagedCache.from_tensors(W.device_cache(g, 2, "cuda", seed=31), "separate")
     ids = rng.permutation(256)[:n].astype(np.int32)
