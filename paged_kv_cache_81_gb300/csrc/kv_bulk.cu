@@ -110,18 +110,53 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity)
     return true;
 }
 
+#ifndef PKV_BULK_EVICT_FIRST
+#define PKV_BULK_EVICT_FIRST 0  // L2 evict-first policy on: 0 none, 1 all bulk copies, 2 unpack's stores, 3 all stores, 4 all loads
+#endif
+
+// L2 policy for data read or written once: evict first (what st.global.cs asks for on the
+// warp engine's stores), so a copy's lines do not displace the next kernel's.
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, uint32_t bytes, uint32_t bar)
 {
+#if PKV_BULK_EVICT_FIRST == 1 || PKV_BULK_EVICT_FIRST == 4
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst_smem),
+        "l"(src), "r"(bytes), "r"(bar), "l"(evict_first_policy())
+        : "memory");
+#else
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      dst_smem),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+#endif
 }
 
+template <bool PACK>
 __device__ __forceinline__ void bulk_store(void *dst, uint32_t src_smem, uint32_t bytes)
 {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
-                 : "memory");
+#if PKV_BULK_EVICT_FIRST == 1 || PKV_BULK_EVICT_FIRST == 3
+    constexpr bool kHint = true;
+#elif PKV_BULK_EVICT_FIRST == 2
+    constexpr bool kHint = !PACK;
+#else
+    constexpr bool kHint = false;
+#endif
+    if (kHint)
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                     "r"(src_smem), "r"(bytes), "l"(evict_first_policy())
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem),
+                     "r"(bytes)
+                     : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -130,7 +165,8 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// The issuing lane's view of one pipe.
+// The issuing lane's view of one pipe (of a pack when PACK, else of an unpack).
+template <bool PACK>
 struct Pipe {
     uint32_t data;  // shared address of slot 0
     PipeState *st;
@@ -149,7 +185,7 @@ struct Pipe {
             pkv::set_error(err, KV_DERR_TIMEOUT);
             return;
         }
-        bulk_store(reinterpret_cast<void *>(st->dst[s]), data + (uint32_t)s * kStage, st->bytes[s]);
+        bulk_store<PACK>(reinterpret_cast<void *>(st->dst[s]), data + (uint32_t)s * kStage, st->bytes[s]);
         bulk_commit();
         head++;
     }
@@ -195,7 +231,7 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
     const int w = threadIdx.x >> 5;
     PipeState *st = reinterpret_cast<PipeState *>(smem + (size_t)kPipes * kSlots * kStage) + w;
 
-    Pipe pipe;
+    Pipe<PACK> pipe;
     pipe.data = smem_addr(smem + (size_t)w * kSlots * kStage);
     pipe.st = st;
     pipe.err = p.err;

@@ -332,14 +332,18 @@ int64_t row_group_ctas(const kv_cache_desc *cache)
     return PKV_RESHAPE_ROWS && g <= kMaxRowGroup ? g : 0;
 }
 
-// CTAs per tensor of a row-write launch: enough for the work, at most about four waves of
-// 8 resident CTAs per SM over the nt tensors of the launch.
+#ifndef PKV_RESHAPE_WAVES
+#define PKV_RESHAPE_WAVES 64  // the row-write grid's cap, in waves of 8 CTAs per SM
+#endif
+
+// CTAs per tensor of a row-write launch: enough for the work, at most about PKV_RESHAPE_WAVES
+// waves of 8 resident CTAs per SM over the nt tensors of the launch.
 void row_grid(const kv_cache_desc *cache, int64_t n_tokens, int32_t nt, const pkv::DeviceInfo &dev, int64_t *need,
               int64_t *cap)
 {
     const int64_t total = n_tokens * cache->n_planes * (cache->row_bytes / 16);
     *need = (total + (int64_t)kRowThreads * kReshapeUnroll - 1) / ((int64_t)kRowThreads * kReshapeUnroll);
-    *cap = std::max<int64_t>(1, ((int64_t)dev.num_sms * 8 * 4 + nt - 1) / nt);
+    *cap = std::max<int64_t>(1, ((int64_t)dev.num_sms * 8 * PKV_RESHAPE_WAVES + nt - 1) / nt);
 }
 
 // Launches shared by kv_reshape_and_cache and kv_write_tokens (arguments already validated).
