@@ -268,14 +268,17 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    t = run_timed(step, dev, stream, args.steps, args.warmup, barrier=barrier, gpu_index=local)
+    # the step as a user issues it (step.run(), no event inside): value and ms_per_step
+    t = run_timed(step, dev, stream, args.steps, args.warmup, barrier=barrier, gpu_index=local, instrument=False)
     elapsed_ms = reduce_max(t["elapsed_ms"], dev)
     b = step.bytes()
     ms_per_step = elapsed_ms / args.steps
     value = world * b.total * args.steps / (elapsed_ms * 1e-3) / 1e9
+    # then the same number of steps with every call bracketed by events: each kernel's duration
+    ti = run_timed(step, dev, stream, args.steps, 0, barrier=barrier, gpu_index=local, instrument=True)
 
     peak, peak_kind = peaks()
-    kernels, per_bytes, per_kernel_ms = kernel_stats(step, t["per_kernel_all"], peak)
+    kernels, per_bytes, per_kernel_ms = kernel_stats(step, ti["per_kernel_all"], peak)
     roofline = roofline_entry(wl.name, per_bytes, per_kernel_ms, peak, peak_kind)
 
     extras = not args.no_extras
@@ -312,6 +315,11 @@ def run_ours(args):
                     "unpack, after both",
         "gpu_launches": args.steps * step.launches_per_step,
         "clocks": t["clocks"],
+        "kernel_timing": {"steps": args.steps, "ms_per_step": round(reduce_max(ti["elapsed_ms"], dev) / args.steps, 4),
+                          "clocks": ti["clocks"],
+                          "how": "value and ms_per_step time K steps issued as step.run() with no event inside a step; "
+                                 "kernels and roofline come from K more steps with CUDA events around every call on "
+                                 "the stream it runs on (the events themselves lengthen that step)"},
         "e2e": e2e,
     }
     if write_path is not None:
@@ -355,14 +363,18 @@ def make_step(wl: W.Workload, case: W.Case, dev, seed: int, **kw):
     return TransferStep(wl, case, src, dst, new, device=dev, **kw)
 
 
-def run_timed(step, dev, stream, steps: int, warmup: int, barrier=lambda: None, gpu_index: int = 0) -> dict:
+def run_timed(step, dev, stream, steps: int, warmup: int, barrier=lambda: None, gpu_index: int = 0,
+              instrument: bool = True) -> dict:
     """W untimed warm-up steps, then exactly K timed steps between CUDA events on `stream`, with a
     synchronize (and the barrier) on both sides and nvidia-smi clocks sampled meanwhile.
 
-    Every call of a step is bracketed by its own events: the builder on the step's second stream
-    (issued first, beside slot_mapping and reshape_and_cache), the rest on `stream`.  A step that
-    moves less than FLUSH_BELOW_BYTES gets an L2-flushing write before it, outside its events, and
-    the elapsed time is then the sum of the steps' own brackets."""
+    instrument=False issues every step as step.run(), the call a user makes, with no event inside
+    it; this pass gives the step time.  instrument=True brackets every call of a step with its own
+    events (the builder on the step's second stream, issued first beside slot_mapping and
+    reshape_and_cache; the rest on `stream`); this pass gives each kernel's duration.  The events
+    cost the step time too (about 20 us of a 1.6 ms page-shaped step).  A step that moves less than
+    FLUSH_BELOW_BYTES gets an L2-flushing write before it, outside its events, and the elapsed time
+    is then the sum of the steps' own start-to-end brackets."""
     import torch
     from paged_kv_cache_81_gb300 import pagedkv as K
 
@@ -419,7 +431,14 @@ def run_timed(step, dev, stream, steps: int, warmup: int, barrier=lambda: None, 
     for s in range(steps):
         if flush:
             flush_buf.fill_(s & 0xFF)  # evicts the previous step's data from L2, outside the step's events
-        timed_step(ev[s])
+        if instrument:
+            timed_step(ev[s])
+        elif flush:
+            ev[s][0].record(stream)
+            step.run(stream)
+            ev[s][5].record(stream)
+        else:
+            step.run(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -431,7 +450,7 @@ def run_timed(step, dev, stream, steps: int, warmup: int, barrier=lambda: None, 
     else:
         elapsed_ms = start.elapsed_time(end)
     per_kernel_all = {name: [ev[s][a].elapsed_time(ev[s][b]) for s in range(steps)]
-                      for name, (a, b) in brackets.items()}
+                      for name, (a, b) in brackets.items()} if instrument else None
     err = K.kv_get_last_error(clear=True)
     if err:
         raise RuntimeError(f"device error word {err:#x} in the timed region")
@@ -487,17 +506,19 @@ def measure_workloads(names, dev, stream, peak: float, peak_kind: str, gpu_index
         wl = W.PRESETS[name]
         case = W.make_case(wl)
         step = make_step(wl, case, dev, wl.seed * 7919)
-        probe = run_timed(step, dev, stream, 3, 3, gpu_index=gpu_index)  # also sizes the timed run
+        probe = run_timed(step, dev, stream, 3, 3, gpu_index=gpu_index, instrument=False)  # sizes the timed run
         per_step_ms = max(probe["elapsed_ms"] / 3, 1e-3)
         steps = int(min(200, max(5, EXTRA_TIMED_S * 1e3 // per_step_ms)))
-        t = run_timed(step, dev, stream, steps, 0, gpu_index=gpu_index)
-        kernels, per_bytes, per_kernel_ms = kernel_stats(step, t["per_kernel_all"], peak)
+        t = run_timed(step, dev, stream, steps, 0, gpu_index=gpu_index, instrument=False)
+        ti = run_timed(step, dev, stream, steps, 0, gpu_index=gpu_index, instrument=True)
+        kernels, per_bytes, per_kernel_ms = kernel_stats(step, ti["per_kernel_all"], peak)
         entry = {"config": config_dict(wl, case, step), "steps": steps,
                  "ms_per_step": round(t["elapsed_ms"] / steps, 4),
                  "value": round(step.bytes().total * steps / (t["elapsed_ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
                  "roofline": roofline_entry(wl.name, per_bytes, per_kernel_ms, peak, peak_kind),
                  "kernels": kernels, "clocks": t["clocks"],
-                 "device_time": "CUDA events around each call on the stream it runs on, every timed step"}
+                 "device_time": "value: the steps issued as step.run() between two CUDA events; kernels: as many "
+                                "steps again with CUDA events around each call on the stream it runs on"}
         if wl.kind == "mla" and step.n_tokens:
             # the decode write is launch-bound: besides its events inside the eager steps above,
             # its device time per write issued back to back from a CUDA graph

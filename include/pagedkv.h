@@ -20,9 +20,11 @@
  *    pointer table) are read during the call only.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and never synchronises, except kv_get_last_error.
- *  - Kernels are launched with programmatic stream serialisation allowed, so their CTAs may
- *    be scheduled while the previous kernel on `stream` still runs; each waits for that
- *    kernel to complete before its first memory access, so the data sees plain stream order.
+ *  - Kernels of a few waves or less are launched with programmatic stream serialisation
+ *    allowed, so their CTAs may be scheduled while the previous kernel on `stream` still runs;
+ *    each waits for that kernel to complete before its first memory access, so the data sees
+ *    plain stream order.  Launches that fill the GPU for longer (pack and unpack with tail
+ *    CTAs, row writes of more than two waves) are plain stream-ordered launches.
  *  - The first call of an entry point on a device sets up per-device state (launch
  *    attributes, occupancy, symbol addresses; the first kv_wait_signal loads every kernel):
  *    make it outside a stream capture.  Calls after it can be captured into CUDA graphs.

@@ -376,7 +376,7 @@ int launch_bulk_copy(const CopyParams &params, int mode, bool pack, const Device
         tail_ctas = std::max<int64_t>(1, std::min<int64_t>((items_max / std::max<int64_t>(1, kTailDiv) + quantum + chunk - 1) / chunk,
                                                            (int64_t)kMaxTailCtasPerResident * p.resident));
     }
-    pkv::launch(fn, p.resident + (int)tail_ctas, kPipes * 32, kSmemBytes, s, p);
+    pkv::launch_as(tail_ctas == 0, fn, p.resident + (int)tail_ctas, kPipes * 32, kSmemBytes, s, p);  // tail: plain
     return cuda_status(cudaGetLastError());
 }
 

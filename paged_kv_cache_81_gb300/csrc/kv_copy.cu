@@ -361,6 +361,7 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     const bool bulk = !host_stage && (mode == MERGED || mode == SPANS) && bulk_engine(piece);
     const KernelFn fn = pick(mode, pack);
     int grid = 0;
+    bool with_tail = false;
     if (!bulk) {
         // persistent CTAs, plus enough tail CTAs for the largest tail the device-side run count
         // allows (a tail CTA whose chunk lies past the items exits at once)
@@ -369,7 +370,7 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
                                   std::min(pkv::kMaxTensorsPerLaunch, cache->n_tensors);
         const int64_t quantum = (int64_t)kWarps * p.resident;
         const int64_t chunk = (int64_t)kWarps * kTailItemsPerWarp;
-        const bool with_tail = kTailDiv > 0 && items_max >= kTailMinItemsPerWarp * quantum;
+        with_tail = kTailDiv > 0 && items_max >= kTailMinItemsPerWarp * quantum;
         p.tail_div = with_tail ? (int32_t)kTailDiv : 0;
         const int64_t tail_ctas = (items_max / std::max<int64_t>(1, kTailDiv) + quantum + chunk - 1) / chunk;
         grid = p.resident + (with_tail ? (int)std::max<int64_t>(1, std::min<int64_t>(tail_ctas, (int64_t)kMaxTailCtasPerResident * p.resident)) : 0);
@@ -385,7 +386,7 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
         if (bulk) {
             st = pkv::launch_bulk_copy(p, mode, pack, *dev, s);
         } else {
-            pkv::launch(fn, grid, kThreads, 0, s, p);
+            pkv::launch_as(!with_tail, fn, grid, kThreads, 0, s, p);  // tail CTAs: a plain launch
             st = pkv::cuda_status(cudaGetLastError());
         }
         if (st != KV_OK) return st;

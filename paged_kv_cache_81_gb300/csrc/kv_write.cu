@@ -346,6 +346,10 @@ void row_grid(const kv_cache_desc *cache, int64_t n_tokens, int32_t nt, const pk
     *cap = std::max<int64_t>(1, ((int64_t)dev.num_sms * 8 * PKV_RESHAPE_WAVES + nt - 1) / nt);
 }
 
+// A row write of at most two waves (of 8 CTAs per SM) takes programmatic dependent launch; a
+// larger one launches plainly (kv_common.cuh, launch_as).
+inline bool pdl_rows(int64_t ctas, const pkv::DeviceInfo &dev) { return ctas <= 2ll * dev.num_sms * 8; }
+
 // Launches shared by kv_reshape_and_cache and kv_write_tokens (arguments already validated).
 template <bool FUSED>
 int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_token_stride, int64_t n_tokens,
@@ -396,10 +400,11 @@ int launch_rows(const kv_cache_desc *cache, const uint64_t *new_kv, int64_t new_
                 if (wave >= row_group && ctas > wave && ctas <= 2 * wave) ctas = wave;
             }
             p.tok_step = (uint32_t)(ctas * kRowThreads / (cache->n_planes * cpr));
-            pkv::launch(FUSED ? reshape_rows_fused_kernel : reshape_rows_kernel, dim3((unsigned)ctas, (unsigned)nt),
-                        kRowThreads, 0, stream, p);
+            pkv::launch_as(pdl_rows(ctas * nt, *dev), FUSED ? reshape_rows_fused_kernel : reshape_rows_kernel,
+                           dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream, p);
         } else {
-            pkv::launch(reshape_and_cache_kernel<FUSED>, dim3((unsigned)ctas, (unsigned)nt), kRowThreads, 0, stream, p);
+            pkv::launch_as(pdl_rows(ctas * nt, *dev), reshape_and_cache_kernel<FUSED>, dim3((unsigned)ctas, (unsigned)nt),
+                           kRowThreads, 0, stream, p);
         }
         st = pkv::cuda_status(cudaGetLastError());
         if (st != KV_OK) return st;
