@@ -1,5 +1,7 @@
 // TMA bulk-copy engine for kv_pack_blocks / kv_unpack_blocks when the cache side is made of
-// contiguous spans: whole runs (MERGED) or one span per (block, plane) (SPANS).
+// contiguous spans: whole runs (MERGED), one span per (block, plane) (SPANS), or, for an unpack
+// onto a block size that is a multiple of the staged one, one span per staged (block, plane) at
+// its destination block's rows (REMAP).
 //
 // Each run of the xfer_list (page "5. flagcx connector design & dev & test", section 1.2:
 // one transfer per contiguous group) becomes one or more bulk copies of at most kStage
@@ -222,7 +224,12 @@ struct Pipe {
     }
 };
 
-template <bool MERGE, bool PACK>
+// MODE: MERGED (a run is one span), SPANS (a span per (block, plane)) or REMAP (unpack onto another
+// block size: a span per (staged block, plane), landing at the rows of the staged block's first
+// token in its destination block; used when the destination's block size is a multiple of the
+// staged one and the slice fills the destination's dense rows, so a staged block never straddles
+// destination blocks).
+template <int MODE, bool PACK>
 __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_constant__ CopyParams p)
 {
     pkv::grid_dep_entry();  // before any global memory access
@@ -280,6 +287,7 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
             if (it < item_end) next = p.runs[it % nr];
         }
         if (lane == 0 && !pipe.failed) {
+            int32_t cached_req = -1, s0 = 0, d0 = 0, dn = 0;  // REMAP: the last request's lists
             for (int i = 0; i < kBatch; i++) {
                 const int64_t item = item_of(round * kBatch + i);
                 if (item >= item_end) break;
@@ -290,6 +298,44 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
                     pkv::set_error(p.err, KV_DERR_STAGE);
                     continue;
                 }
+                if (MODE == pkv::REMAP) {
+                    const int32_t r = run.req;
+                    if (r < 0 || r >= p.n_reqs) {
+                        pkv::set_error(p.err, KV_DERR_DST_TABLE);
+                        continue;
+                    }
+                    if (r != cached_req) {
+                        cached_req = r;
+                        s0 = p.src_req_offsets[r];
+                        d0 = p.dst_req_offsets[r];
+                        dn = p.dst_req_offsets[r + 1] - d0;
+                    }
+                    if (run.stage_block < s0 || dn < 0 || d0 < 0) {  // offsets that do not match the runs
+                        pkv::set_error(p.err, KV_DERR_DST_TABLE);
+                        continue;
+                    }
+                    uint8_t *const cache_t = reinterpret_cast<uint8_t *>(p.base[t]);
+                    const int64_t planes = block_bytes / span_bytes;
+                    for (int32_t m = 0; m < run.n_blocks; m++) {
+                        const int64_t j = (run.stage_block - s0 + m) * (int64_t)p.div_bs.d;  // its first token
+                        const int64_t dq = j / p.div_dbs.d;
+                        if (dq >= dn) {
+                            pkv::set_error(p.err, KV_DERR_DST_TABLE);
+                            continue;
+                        }
+                        const int32_t db = p.dst_ids[d0 + dq];
+                        if (db < 0 || db >= p.num_blocks) {
+                            pkv::set_error(p.err, KV_DERR_BLOCK);
+                            continue;
+                        }
+                        uint8_t *const dst = cache_t + (int64_t)db * p.block_stride + (j - dq * p.div_dbs.d) * p.token_stride;
+                        const uint8_t *const src = p.stage + (int64_t)(p.tensor_begin + t) * p.stage_tensor_bytes +
+                                                   (run.stage_block + m) * block_bytes;
+                        for (int64_t pl = 0; pl < planes; pl++)
+                            pipe.span(src + pl * span_bytes, dst + pl * p.plane_stride, span_bytes);
+                    }
+                    continue;
+                }
                 const int64_t blk = PACK ? run.src_block : run.dst_block;
                 if (blk < 0 || blk + run.n_blocks > p.num_blocks) {
                     pkv::set_error(p.err, KV_DERR_BLOCK);
@@ -298,7 +344,7 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
                 uint8_t *const cache = reinterpret_cast<uint8_t *>(p.base[t]) + blk * p.block_stride;
                 uint8_t *const stage =
                     p.stage + (int64_t)(p.tensor_begin + t) * p.stage_tensor_bytes + run.stage_block * block_bytes;
-                if (MERGE) {
+                if (MODE == pkv::MERGED) {
                     const int64_t bytes = (int64_t)run.n_blocks * block_bytes;
                     if (PACK) pipe.span(cache, stage, bytes);
                     else pipe.span(stage, cache, bytes);
@@ -330,8 +376,9 @@ using BulkFn = void (*)(CopyParams);
 
 BulkFn pick(int mode, bool pack)
 {
-    if (mode == pkv::MERGED) return pack ? bulk_copy_kernel<true, true> : bulk_copy_kernel<true, false>;
-    return pack ? bulk_copy_kernel<false, true> : bulk_copy_kernel<false, false>;
+    if (mode == pkv::MERGED) return pack ? bulk_copy_kernel<pkv::MERGED, true> : bulk_copy_kernel<pkv::MERGED, false>;
+    if (mode == pkv::REMAP) return bulk_copy_kernel<pkv::REMAP, false>;
+    return pack ? bulk_copy_kernel<pkv::SPANS, true> : bulk_copy_kernel<pkv::SPANS, false>;
 }
 
 }  // namespace
@@ -340,18 +387,19 @@ namespace pkv {
 
 int preload_bulk_kernels()
 {
-    return load_kernels(bulk_copy_kernel<true, true>, bulk_copy_kernel<true, false>, bulk_copy_kernel<false, true>,
-                        bulk_copy_kernel<false, false>);
+    return load_kernels(bulk_copy_kernel<pkv::MERGED, true>, bulk_copy_kernel<pkv::MERGED, false>,
+                        bulk_copy_kernel<pkv::SPANS, true>, bulk_copy_kernel<pkv::SPANS, false>,
+                        bulk_copy_kernel<pkv::REMAP, false>);
 }
 
 int launch_bulk_copy(const CopyParams &params, int mode, bool pack, const DeviceInfo &dev, cudaStream_t s)
 {
     CopyParams p = params;
     static std::mutex mu;
-    static bool configured[64][2][2];
-    static int per_sm[64][2][2];
+    static bool configured[64][3][2];
+    static int per_sm[64][3][2];
     const BulkFn fn = pick(mode, pack);
-    const int m = mode == MERGED ? 1 : 0, d = pack ? 1 : 0, di = dev.device & 63;
+    const int m = mode == MERGED ? 1 : mode == REMAP ? 2 : 0, d = pack ? 1 : 0, di = dev.device & 63;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!configured[di][m][d]) {

@@ -357,8 +357,12 @@ int launch(const kv_cache_desc *cache, const kv_stage_desc *stage, int mode, boo
     p.max_pieces = max_run_blocks > 0 ? (int32_t)std::min<int64_t>((run_chunks + kPieceChunks - 1) / kPieceChunks, 1 << 20) : 1;
 
     // staging in host memory goes over the host link with the warp engine's 16-byte accesses
-    const int64_t piece = mode == SPANS ? stage_block_bytes / stage->n_planes : stage_block_bytes;
-    const bool bulk = !host_stage && (mode == MERGED || mode == SPANS) && bulk_engine(piece);
+    const int64_t piece = mode == MERGED ? stage_block_bytes : stage_block_bytes / stage->n_planes;
+    // a remap whose staged blocks land whole inside destination blocks, on rows the slice fills,
+    // is one span per staged (block, plane)
+    const bool remap_spans = mode == REMAP && row_off == 0 && cache->row_bytes == stage->slice_bytes &&
+                             cache->token_stride == stage->slice_bytes && dst_block_size % stage->block_size == 0;
+    const bool bulk = !host_stage && (mode == MERGED || mode == SPANS || remap_spans) && bulk_engine(piece);
     const KernelFn fn = pick(mode, pack);
     int grid = 0;
     bool with_tail = false;
