@@ -199,14 +199,17 @@ def test_copy_engine_layouts(layout, heads, engine):
     G.compare(gpu, ora, wl.name)
 
 
-@pytest.mark.parametrize("layout,bs,dst_bs,head_dim,extra,engine", [
-    ("separate", 16, 64, 128, 0, "tma"),       # 4 KiB staged blocks landing whole in 64-slot blocks
-    ("blocks_first", 16, 32, 128, 0, "tma"),   # two planes: a span per (staged block, plane)
-    ("separate", 16, 64, 128, 32, "warp"),     # the slice inside a wider destination row
-    ("separate", 16, 24, 128, 0, "warp"),      # 24 is not a multiple of 16: staged blocks straddle
-    ("separate", 8, 32, 64, 0, "warp"),        # 8 x 128 B = 1 KiB spans: below the TMA engine's 4 KiB
-], ids=["tma_1plane", "tma_2planes", "warp_wider_row", "warp_straddle", "warp_small_span"])
-def test_remap_engines(layout, bs, dst_bs, head_dim, extra, engine):
+@pytest.mark.parametrize("layout,dst_layout,bs,dst_bs,head_dim,extra,engine", [
+    ("separate", "separate", 16, 64, 128, 0, "tma"),          # 4 KiB staged blocks landing whole in 64-slot blocks
+    ("blocks_first", "blocks_first", 16, 32, 128, 0, "tma"),  # two planes: a span per (staged block, plane)
+    ("kv_first", "kv_first", 16, 64, 128, 0, "tma"),          # planes a whole cache apart
+    ("blocks_first", "kv_first", 32, 64, 64, 0, "tma"),       # the two layer layouts of the drawing, mixed
+    ("separate", "separate", 16, 64, 128, 32, "warp"),        # the slice inside a wider destination row
+    ("separate", "separate", 16, 24, 128, 0, "warp"),         # 24 is not a multiple of 16: staged blocks straddle
+    ("separate", "separate", 8, 32, 64, 0, "warp"),           # 8 x 128 B = 1 KiB spans: below the TMA engine's 4 KiB
+], ids=["tma_1plane", "tma_2planes", "tma_kv_first", "tma_mixed_layouts", "warp_wider_row", "warp_straddle",
+        "warp_small_span"])
+def test_remap_engines(layout, dst_layout, bs, dst_bs, head_dim, extra, engine):
     """Unpack onto another block size on both copy engines, against the oracle.  A remap whose
     staged blocks land whole inside destination blocks (the destination block size a multiple of
     the staged one) on rows the slice fills takes the TMA engine when a (block, plane) span is 4 KiB
@@ -214,7 +217,7 @@ def test_remap_engines(layout, bs, dst_bs, head_dim, extra, engine):
     from dataclasses import replace
     row = head_dim * 2
     src = W.CacheGeom(layout, 160, bs, 1, head_dim)
-    dst = W.CacheGeom(layout, 160 * bs // dst_bs + 8, dst_bs, 1, head_dim + extra // 2)
+    dst = W.CacheGeom(dst_layout, 160 * bs // dst_bs + 8, dst_bs, 1, head_dim + extra // 2)
     span = bs * row
     assert ((span >= 4096 and dst_bs % bs == 0 and extra == 0) == (engine == "tma"))
     wl = replace(W.TINY, name=f"remap_{layout}_{bs}_{dst_bs}_{extra}", src=src, dst=dst,
