@@ -22,9 +22,6 @@
 
 #include "kv_common.cuh"
 
-#ifndef PKV_HASH_W128
-#define PKV_HASH_W128 1  // 0: the table kernel loads each byte's weight on its own
-#endif
 #ifndef PKV_HASH_PDL
 #define PKV_HASH_PDL 1  // 0: plain stream-ordered launches for every hash kernel
 #endif
@@ -77,12 +74,13 @@ __device__ __forceinline__ Fnv fnv_block_start(uint64_t parent)
     return fnv_bytes<8>(Fnv{(uint32_t)kFnvBasis, (uint32_t)(kFnvBasis >> 32)}, parent);
 }
 
-__global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
-                                                                  int32_t n_tokens, int32_t bs, int32_t *out_off,
-                                                                  int *err)
+// The full-block count of every request scanned into the output CSR offsets by one CTA of
+// THREADS threads (also flags offsets that do not describe n_tokens tokens).
+template <int THREADS>
+__device__ void count_blocks(const int32_t *__restrict__ off, int32_t n_reqs, int32_t n_tokens, int32_t bs,
+                             int32_t *out_off, int *err)
 {
-    pkv::grid_dep_entry();  // before any global memory access
-    __shared__ int32_t warp_sum[kScanThreads / 32];
+    __shared__ int32_t warp_sum[THREADS / 32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -90,7 +88,7 @@ __global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t 
         if (off[0] != 0 || off[n_reqs] != n_tokens) pkv::set_error(err, KV_DERR_LIST);
     }
     __syncthreads();
-    for (int32_t base = 0; base < n_reqs; base += kScanThreads) {
+    for (int32_t base = 0; base < n_reqs; base += THREADS) {
         const int32_t r = base + tid;
         int32_t cnt = 0;
         if (r < n_reqs) {
@@ -107,7 +105,7 @@ __global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t 
         if (lane == 31) warp_sum[warp] = incl;
         __syncthreads();
         int32_t before = 0, total = 0;
-        for (int w = 0; w < kScanThreads / 32; w++) {
+        for (int w = 0; w < THREADS / 32; w++) {
             if (w < warp) before += warp_sum[w];
             total += warp_sum[w];
         }
@@ -117,6 +115,14 @@ __global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t 
         __syncthreads();
     }
     if (tid == 0) out_off[n_reqs] = carry;
+}
+
+__global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
+                                                                  int32_t n_tokens, int32_t bs, int32_t *out_off,
+                                                                  int *err)
+{
+    pkv::grid_dep_entry();  // before any global memory access
+    count_blocks<kScanThreads>(off, n_reqs, n_tokens, bs, out_off, err);
 }
 
 // Request r's span, block count and first hash index; false (and KV_DERR_LIST where the output
@@ -177,15 +183,22 @@ __global__ void __launch_bounds__(kChainThreads) hash_chain_kernel(const int32_t
 }
 
 // ---- with a workspace: tables of D, then the walk ----
-constexpr int kTableThreads = 256;  // one thread per starting low byte c
-constexpr int kTableChunk = 512;    // tokens staged in shared memory at a time
-#ifndef PKV_HASH_RING
-#define PKV_HASH_RING 8
+constexpr int kTableThreads = 256;  // one thread per table entry
+constexpr int kTableChunk = 512;    // tokens per Horner chunk
+constexpr int kTableGroup = 16;     // token loads issued ahead of their bytes
+constexpr int kOffCache = 1024;     // request offsets a table CTA keeps in shared memory
+constexpr int kFusedScanMaxReqs = 4096;  // up to this many requests, table CTA 0 also scans the counts
+constexpr uint32_t kTableBytes = 256 * sizeof(uint64_t);
+#ifndef PKV_HASH_SEG
+#define PKV_HASH_SEG 16  // tables per bulk copy of the walk
 #endif
-#ifndef PKV_HASH_BATCH
-#define PKV_HASH_BATCH 4
+#ifndef PKV_HASH_SEGS
+#define PKV_HASH_SEGS 4  // segments in the walk's shared-memory ring
 #endif
-constexpr int kRing = PKV_HASH_RING;  // tables in flight per walking warp
+constexpr int kSeg = PKV_HASH_SEG;
+constexpr int kSegs = PKV_HASH_SEGS;
+static_assert(kSeg >= 1 && kSeg <= 32 && kSegs >= 2, "walk ring shape");
+constexpr uint32_t kWalkSmem = (uint32_t)(kSegs * kSeg + 1) * kTableBytes;  // + room to align the ring to 2 KiB
 
 // 64-bit arithmetic modulo 2^64 for the table weights.
 __host__ __device__ constexpr uint64_t pow_mod_2_64(uint64_t base, uint64_t e)
@@ -214,10 +227,9 @@ struct SplitWeight {
     int32_t lo_s;
     uint32_t hi;
 };
-__device__ __forceinline__ SplitWeight split_weight(uint64_t w)
+__host__ __device__ constexpr SplitWeight split_weight(uint64_t w)
 {
-    const uint32_t lo = (uint32_t)w;
-    return SplitWeight{(int32_t)lo, (uint32_t)(w >> 32) + (lo >> 31)};
+    return SplitWeight{(int32_t)(uint32_t)w, (uint32_t)(w >> 32) + ((uint32_t)w >> 31)};
 }
 __device__ __forceinline__ uint64_t join_weight(SplitWeight s)
 {
@@ -225,152 +237,250 @@ __device__ __forceinline__ uint64_t join_weight(SplitWeight s)
     return ((uint64_t)(s.hi - (lo >> 31)) << 32) | lo;
 }
 
-// Block g's table: D[c] for c = threadIdx.x.  Blocks are numbered by their hash index; a CTA
-// takes blocks g = blockIdx.x, + gridDim.x, ... below min(hash count, limit).
-// D = sum_k P^(n-k) d_k is taken as a weighted sum over the block's bytes in chunks of at most
-// kTableChunkBytes, joined by Horner (D <- D * P^(chunk bytes) + chunk sum).  The weights
-// P^(M - i), M = min(n, kTableChunkBytes), are computed once per CTA into shared memory; a
-// chunk of m bytes uses the last m of them.  Per byte: a byte extract and xor, one
-// subtraction, a signed 32x32->64 multiply-add, a 32-bit multiply-add, and the chain's multiply.
+// Table layout.  Blocks are keyed by their slot, floor(first token / block size): a request's
+// blocks then have consecutive slots, and no two blocks share one (request r's blocks end at
+// or before off[r + 1], where the next request's first slot begins), so the tables fit in
+// n_tokens / block size slots with no need for the output offsets.  Slot i's table holds, at
+// entry x, D[(x * P) mod 256]: the entry for the state's low byte before the last multiply of
+// the parent bytes, which saves the walk that multiply.
+//
+// The table kernel: slot i, i = blockIdx.x, + gridDim.x, ...; the block (if any) that starts
+// in tokens [i * bs, (i + 1) * bs) belongs to the request holding token (i + 1) * bs - 1.
+// D = sum_k P^(n-k) d_k is a weighted sum over the block's bytes in chunks of at most
+// kTableChunk tokens, joined by Horner (D <- D * P^(chunk bytes) + chunk sum).  The weights
+// P^(M - i), M = min(n, 4 kTableChunk), are computed once per CTA into shared memory; a chunk
+// of m bytes uses the last m of them.  Per byte: a byte extract and xor, one subtraction, a
+// signed 32x32->64 multiply-add, a 32-bit multiply-add, and the chain's multiply.  Tokens are
+// read straight from global memory (the same address across the CTA), so a slot needs no
+// barrier.  When scan is set, CTA 0 first writes the output offsets.
 constexpr int kTableChunkBytes = 4 * kTableChunk;
 
 __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
                                                                    const int32_t *__restrict__ tokens,
-                                                                   int32_t n_tokens, int32_t bs,
-                                                                   const int32_t *__restrict__ out_off,
-                                                                   uint64_t *__restrict__ table, int64_t limit)
+                                                                   int32_t n_tokens, int32_t bs, int32_t *out_off,
+                                                                   uint64_t *__restrict__ table, int32_t n_slots,
+                                                                   pkv::FastDiv div_bs, bool scan, int *err)
 {
     pkv::grid_dep_entry();  // before any global memory access
-    __shared__ uint32_t sh_tok[kTableChunk];
     __shared__ __align__(16) SplitWeight sh_w[kTableChunkBytes];
-    const int64_t n_hash = min((int64_t)out_off[n_reqs], limit);
-    const uint32_t c0 = threadIdx.x;
+    __shared__ int32_t sh_off[kOffCache + 1];
+    if (scan && blockIdx.x == 0) count_blocks<kTableThreads>(off, n_reqs, n_tokens, bs, out_off, err);
+    const int tid = threadIdx.x;
+    const bool cached = n_reqs <= kOffCache;
+    if (cached)
+        for (int i = tid; i <= n_reqs; i += kTableThreads) sh_off[i] = off[i];
     const int32_t nb = 4 * bs;  // token bytes per block
     const int32_t M = min(nb, kTableChunkBytes);
-    if ((int32_t)c0 < M) {
-        uint64_t w = pow_mod_2_64(kFnvPrime, (uint64_t)(M - (int32_t)c0));
-        for (int32_t i = c0; i < M; i += kTableThreads) {
+    if (tid < M) {
+        uint64_t w = pow_mod_2_64(kFnvPrime, (uint64_t)(M - tid));
+        for (int32_t i = tid; i < M; i += kTableThreads) {
             sh_w[i] = split_weight(w);  // P^(M - i)
             w *= kPrimeInvPow256;       // P^(M - i - 256)
         }
     }
-    for (int64_t g = blockIdx.x; g < n_hash; g += gridDim.x) {
-        int32_t lo = 0, hi = n_reqs - 1;  // the request holding hash g: last r with out_off[r] <= g
+    __syncthreads();
+    const uint32_t c0 = ((uint32_t)tid * 0xb3u) & 0xffu;  // this thread's low byte of the state
+    for (int32_t i = blockIdx.x; i < n_slots; i += gridDim.x) {
+        const int64_t t = (int64_t)i * bs;
+        const int64_t last = t + bs - 1;
+        int32_t lo = 0, hi = n_reqs - 1;  // the last request r with off[r] <= last
         while (lo < hi) {
             const int32_t mid = (lo + hi + 1) >> 1;
-            if (out_off[mid] <= g) lo = mid;
+            if ((cached ? sh_off[mid] : off[mid]) <= last) lo = mid;
             else hi = mid - 1;
         }
-        const int32_t begin = off[lo];
-        const int64_t first = (int64_t)begin + (g - out_off[lo]) * (int64_t)bs;  // the block's first token
-        const bool ok = begin >= 0 && first >= 0 && first + bs <= n_tokens && off[lo + 1] - begin >= 0;
+        const int64_t o = cached ? sh_off[lo] : off[lo];
+        const int64_t o1 = cached ? sh_off[lo + 1] : off[lo + 1];
+        if (o > last) continue;  // (offsets out of order)
+        // the one token of the window at a block boundary of r: o + floor((last - o) / bs) * bs
+        const int64_t first = o + (int64_t)pkv::fdiv((uint32_t)(last - o), div_bs) * bs;
+        if (first + bs > o1 || first + bs > n_tokens) continue;  // no block starts here
+        const int32_t *tp = tokens + first;
         uint32_t c = c0;
         uint64_t D = 0;
         for (int32_t j0 = 0; j0 < bs; j0 += kTableChunk) {
             const int32_t m = min(kTableChunk, bs - j0);
             const SplitWeight *w = sh_w + (M - 4 * m);
-            __syncthreads();  // the previous chunk has been read (and, the first time, the weights written)
-            for (int q = threadIdx.x; q < m; q += kTableThreads) sh_tok[q] = ok ? (uint32_t)tokens[first + j0 + q] : 0u;
-            __syncthreads();
             int64_t acc = 0;
             uint32_t acc_hi = 0;
             // c keeps the product's high bits: x and c then share all but their low byte, so
             // x - c is still the low bytes' difference, and x's low byte alone sets c's next one.
-#pragma unroll 2
-            for (int q = 0; q < m; q++) {
-                const uint32_t v = sh_tok[q];
-#if PKV_HASH_W128
+            auto token = [&](uint32_t v, int32_t q) {
                 // a token's 4 weights are 32 contiguous bytes (w + 4q is 32-byte aligned: chunks
-                // start at a multiple of 4 weights): two 16-byte loads instead of four 8-byte ones
+                // start at a multiple of 4 weights): two 16-byte loads
                 const uint4 w01 = *reinterpret_cast<const uint4 *>(w + 4 * q);
                 const uint4 w23 = *reinterpret_cast<const uint4 *>(w + 4 * q + 2);
                 const uint32_t wl[4] = {w01.x, w01.z, w23.x, w23.z}, wh[4] = {w01.y, w01.w, w23.y, w23.w};
-#endif
 #pragma unroll
                 for (int byte = 0; byte < 4; byte++) {
                     const uint32_t x = c ^ ((v >> (8 * byte)) & 0xffu);
                     const int32_t d = (int32_t)x - (int32_t)c;
-#if PKV_HASH_W128
                     acc += (int64_t)d * (int32_t)wl[byte];
                     acc_hi += (uint32_t)d * wh[byte];
-#else
-                    const SplitWeight wk = w[4 * q + byte];
-                    acc += (int64_t)d * wk.lo_s;
-                    acc_hi += (uint32_t)d * wk.hi;
-#endif
                     c = x * 0x1b3u;
                 }
+            };
+            int32_t q = 0;
+            for (; q + kTableGroup <= m; q += kTableGroup) {
+                uint32_t v[kTableGroup];
+#pragma unroll
+                for (int g = 0; g < kTableGroup; g++) v[g] = (uint32_t)__ldg(tp + j0 + q + g);
+#pragma unroll
+                for (int g = 0; g < kTableGroup; g++) token(v[g], q + g);
             }
+            for (; q < m; q++) token((uint32_t)__ldg(tp + j0 + q), q);
             D = D * join_weight(w[0]) + (uint64_t)acc + ((uint64_t)acc_hi << 32);
         }
-        table[g * 256 + c0] = D;
+        table[(int64_t)i * 256 + tid] = D;
     }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t smem, const void *gmem)
+// The walk's constants for n token bytes per block: the hash of a block is
+//     H = K0 + sum_{k<8} W_k e_k + T[x]
+// with K0 = P^(n+8) basis, W_k = P^(n+8-k), e_k the k-th parent byte's low-byte difference
+// (the state is P^8 basis + sum_k P^(8-k) e_k after the parent bytes, and the tokens then
+// multiply it by P^n) and T the slot's table at x, the low byte before the last multiply.
+struct WalkConsts {
+    uint64_t k0;
+    SplitWeight w[8];
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long now_ns()
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// One warp per request (one warp per CTA).  The warp keeps the tables of the next kRing blocks
-// in flight in a shared-memory ring (cp.async, 64 bytes per lane per table, kBatch tables per
-// commit group) while every lane runs the same serial chain; the table entry is a broadcast
-// shared load.
-constexpr int kBatch = PKV_HASH_BATCH;
-static_assert(kRing % kBatch == 0, "the ring holds whole groups");
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
+// Bounded wait (2 s of globaltimer) for the phase with the given parity; false when it ran out.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = now_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (now_ns() - t0 > 2000000000ull) return false;
+    return true;
+}
+
+// One block of the walk from parent h; tab is the shared address of the block's table (2 KiB
+// aligned).  The critical path is the low-byte chain of the parent's bytes (an xor and a
+// multiply per byte), the table load and an add; the rest of H is summed beside it.  The
+// chain's value keeps the product's high bits, which the xor with a byte leaves alone, so
+// x - c is exact.  The last multiply uses 8 P, putting the low byte at bits 3..10 where it is
+// the table entry's byte offset.
+__device__ __forceinline__ uint64_t walk_block(uint64_t h, const WalkConsts &wc, uint32_t tab)
+{
+    const uint32_t lo = (uint32_t)h, hi = (uint32_t)(h >> 32);
+    uint32_t c = (uint32_t)kFnvBasis;
+    int32_t e[8];
+#pragma unroll
+    for (int k = 0; k < 7; k++) {
+        const uint32_t x = c ^ (((k < 4 ? lo : hi) >> (8 * (k & 3))) & 0xffu);
+        e[k] = (int32_t)(x - c);
+        c = x * (k < 6 ? 0x1b3u : 8u * 0x1b3u);
+    }
+    const uint32_t p7 = (hi >> 21) & 0x7f8u;  // the last parent byte, times 8
+    e[7] = (int32_t)((c ^ p7) - c) >> 3;
+    const uint32_t addr = (c & 0x7f8u) ^ (p7 | tab);  // tab + 8 * (the low byte after the xor)
+    uint64_t t;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(t) : "r"(addr));
+    int64_t acc = (int64_t)wc.k0;
+    uint32_t acc_hi = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        acc += (int64_t)e[k] * wc.w[k].lo_s;
+        acc_hi += (uint32_t)e[k] * wc.w[k].hi;
+    }
+    return (uint64_t)acc + ((uint64_t)acc_hi << 32) + t;
+}
+
+// One warp per request (one warp per CTA).  Lane 0 copies the request's tables into a ring of
+// kSegs segments of kSeg tables, one bulk copy (cp.async.bulk, completion counted on the
+// segment's mbarrier) per segment, kSegs - 1 segments ahead of the walk.  Every lane runs the
+// same chain; lane q keeps the q-th hash of a segment, and lanes 0 .. kSeg - 1 store them
+// together.  A wait that runs out (2 s) sets KV_DERR_TIMEOUT; the CTA then waits, bounded
+// again, for its copies still in flight and returns.
 __global__ void __launch_bounds__(32) hash_walk_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
-                                                       int32_t n_tokens, int32_t bs, uint64_t seed, uint64_t p_pow_n,
+                                                       int32_t n_tokens, int32_t bs, uint64_t seed,
+                                                       const __grid_constant__ WalkConsts wc,
                                                        const int32_t *__restrict__ out_off,
                                                        const uint64_t *__restrict__ table, int64_t limit,
                                                        uint64_t *__restrict__ out, int *err)
 {
     pkv::grid_dep_entry();  // before any global memory access
-    constexpr int kGroups = kRing / kBatch;  // commit groups in flight
-    extern __shared__ __align__(16) uint64_t ring_mem[];  // kRing tables of 256 entries
-    uint64_t(*ring)[256] = reinterpret_cast<uint64_t(*)[256]>(ring_mem);
+    extern __shared__ __align__(16) uint8_t walk_smem[];
+    __shared__ __align__(8) uint64_t bar[kSegs];
     const int lane = threadIdx.x;
-    const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(ring_mem);
+    const uint32_t ring = (smem_addr(walk_smem) + kTableBytes - 1) & ~(kTableBytes - 1);
+    if (lane == 0) {
+        for (int s = 0; s < kSegs; s++)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    uint32_t parity = 0;  // bit s: the parity of segment slot s's next phase
     for (int32_t r = blockIdx.x; r < n_reqs; r += gridDim.x) {
         int32_t begin, k;
         int64_t at;
         if (!request_blocks(off, r, n_tokens, bs, out_off, limit, err, &begin, &k, &at)) continue;
-        const uint64_t *tab = table + at * 256;
-        auto fetch = [&](int32_t j0) {  // tables j0 .. j0 + kBatch - 1 into their ring slots, one group
-#pragma unroll
-            for (int q = 0; q < kBatch; q++) {
-                const int32_t j = j0 + q;
-                if (j < k) {
-                    const char *src = reinterpret_cast<const char *>(tab + (int64_t)j * 256) + lane * 64;
-                    const uint32_t dst = ring_base + (uint32_t)((j % kRing) * 2048 + lane * 64);
-#pragma unroll
-                    for (int w = 0; w < 4; w++) cp_async16(dst + w * 16, src + w * 16);
-                }
-            }
-            cp_async_commit();
+        const uint64_t *tab = table + (int64_t)(begin / bs) * 256;
+        const int32_t nseg = (k + kSeg - 1) / kSeg;
+        auto issue = [&](int32_t s) {  // segment s into its ring slot, issued by lane 0 (predicated, no branch)
+            const uint32_t slot = (uint32_t)(s % kSegs);
+            const uint32_t bytes = (uint32_t)min(kSeg, k - s * kSeg) * kTableBytes;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.eq.u32 p, %0, 0;\n\t"
+                "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t"
+                "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%3], [%4], %2, [%1];\n\t}" ::"r"(
+                    lane),
+                "r"(smem_addr(&bar[slot])), "r"(bytes), "r"(ring + slot * (uint32_t)(kSeg * kTableBytes)),
+                "l"(tab + (int64_t)s * kSeg * 256)
+                : "memory");
         };
-#pragma unroll
-        for (int g = 0; g < kGroups; g++) fetch(g * kBatch);
-        uint64_t parent = seed;
-        for (int32_t j0 = 0; j0 < k; j0 += kBatch) {
-            cp_async_wait<kGroups - 1>();  // this lane's copies of tables j0 .. j0 + kBatch - 1 have landed
-            __syncwarp();                  // and every other lane's
-#pragma unroll
-            for (int q = 0; q < kBatch; q++) {
-                const int32_t j = j0 + q;
-                if (j >= k) break;
-                const Fnv S = fnv_block_start(parent);
-                parent = p_pow_n * fnv_value(S) + ring[j % kRing][S.lo & 0xffu];
-                if (lane == 0) out[at + j] = parent;
+        for (int32_t s = 0; s < min(nseg, kSegs); s++) issue(s);
+        uint64_t h = seed;
+        for (int32_t s = 0; s < nseg; s++) {
+            const uint32_t slot = (uint32_t)(s % kSegs);
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar[slot]), (parity >> slot) & 1u))) {
+                // let the copies still in flight (this one included) land before shared memory goes away
+                if (lane == 0) pkv::set_error(err, KV_DERR_TIMEOUT);
+                for (int32_t s2 = s; s2 < min(nseg, s + kSegs); s2++) {
+                    const uint32_t sl = (uint32_t)(s2 % kSegs);
+                    mbar_wait(smem_addr(&bar[sl]), (parity >> sl) & 1u);
+                    parity ^= 1u << sl;
+                }
+                return;
             }
-            __syncwarp();  // the group's slots are read by all lanes before they are refilled
-            fetch(j0 + kRing);
+            parity ^= 1u << slot;
+            const uint32_t seg = ring + slot * (uint32_t)(kSeg * kTableBytes);
+            const int32_t j0 = s * kSeg;
+            uint64_t keep = 0;
+#pragma unroll
+            for (int q = 0; q < kSeg; q++) {
+                if (j0 + q >= k) break;
+                h = walk_block(h, wc, seg + (uint32_t)q * kTableBytes);
+                if (lane == q) keep = h;
+            }
+            if (lane < kSeg && j0 + lane < k) out[at + j0 + lane] = keep;
+            __syncwarp();  // every lane has read the segment before it is refilled
+            if (s + kSegs < nseg) issue(s + kSegs);
         }
-        cp_async_wait<0>();
-        __syncwarp();
     }
 }
 
@@ -410,10 +520,16 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
     if (dev == nullptr) return KV_ERR_CUDA;
     const cudaStream_t s = (cudaStream_t)stream;
     if (n_reqs == 0) return pkv::cuda_status(cudaMemsetAsync(out_offsets, 0, sizeof(int32_t), s));
-    pkv::launch<kHashPdl>(hash_count_kernel, 1, kScanThreads, 0, s, tok_offsets, n_reqs, (int32_t)n_tokens, block_size,
-                          out_offsets, dev->err_word);
-    int st = pkv::cuda_status(cudaGetLastError());
-    if (st != KV_OK) return st;
+    const int32_t n_slots = (int32_t)(n_tokens / block_size);  // out_capacity >= n_slots (checked above)
+    const bool table_path = workspace != nullptr && n_slots > 0;
+    const bool fused_scan = table_path && n_reqs <= kFusedScanMaxReqs;
+    int st = KV_OK;
+    if (!fused_scan) {
+        pkv::launch<kHashPdl>(hash_count_kernel, 1, kScanThreads, 0, s, tok_offsets, n_reqs, (int32_t)n_tokens,
+                              block_size, out_offsets, dev->err_word);
+        st = pkv::cuda_status(cudaGetLastError());
+        if (st != KV_OK) return st;
+    }
     if (workspace == nullptr) {
         const int blocks = std::max(1, std::min((n_reqs + kChainThreads - 1) / kChainThreads, dev->num_sms * 4));
         pkv::launch<kHashPdl>(hash_chain_kernel, blocks, kChainThreads, 0, s, tok_offsets, n_reqs, tokens,
@@ -421,31 +537,32 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
                               dev->err_word);
         return pkv::cuda_status(cudaGetLastError());
     }
-    // hashes beyond n_tokens / block_size only arise from inconsistent offsets (flagged by the count)
-    const int64_t limit = std::min<int64_t>(out_capacity, n_tokens / block_size);
-    if (limit == 0) return KV_OK;
+    if (n_slots == 0) return KV_OK;
     uint64_t *table = reinterpret_cast<uint64_t *>(workspace);
-    const int table_blocks = (int)std::min<int64_t>(limit, (int64_t)dev->num_sms * 8);
+    const int table_blocks = std::min(n_slots, dev->num_sms * 8);
     pkv::launch<kHashPdl>(hash_table_kernel, table_blocks, kTableThreads, 0, s, tok_offsets, n_reqs, tokens,
-                          (int32_t)n_tokens, block_size, out_offsets, table, limit);
+                          (int32_t)n_tokens, block_size, out_offsets, table, n_slots, pkv::make_fastdiv((uint32_t)block_size),
+                          fused_scan, dev->err_word);
     st = pkv::cuda_status(cudaGetLastError());
     if (st != KV_OK) return st;
-    const uint64_t p_pow_n = pow_mod_2_64(kFnvPrime, 4ull * (uint64_t)block_size);
-    constexpr int kRingBytes = kRing * 256 * (int)sizeof(uint64_t);
+    WalkConsts wc{};
+    const uint64_t n8 = 4ull * (uint64_t)block_size + 8;  // bytes hashed per block
+    wc.k0 = pow_mod_2_64(kFnvPrime, n8) * kFnvBasis;
+    for (int k = 0; k < 8; k++) wc.w[k] = split_weight(pow_mod_2_64(kFnvPrime, n8 - (uint64_t)k));
     static std::mutex mu;
     static bool configured[64];
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (kRingBytes > 48 * 1024 && !configured[dev->device & 63]) {
+        if (kWalkSmem > 48 * 1024 && !configured[dev->device & 63]) {
             st = pkv::cuda_status(
-                cudaFuncSetAttribute(hash_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes));
+                cudaFuncSetAttribute(hash_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWalkSmem));
             if (st != KV_OK) return st;
             configured[dev->device & 63] = true;
         }
     }
     const int walk_blocks = std::min(n_reqs, dev->num_sms * 16);
-    pkv::launch<kHashPdl && PKV_HASH_WALK_PDL>(hash_walk_kernel, walk_blocks, 32, kRingBytes, s, tok_offsets, n_reqs,
-                                               (int32_t)n_tokens, block_size, seed, p_pow_n, out_offsets, table, limit,
-                                               out_hashes, dev->err_word);
+    pkv::launch<kHashPdl && PKV_HASH_WALK_PDL>(hash_walk_kernel, walk_blocks, 32, kWalkSmem, s, tok_offsets, n_reqs,
+                                               (int32_t)n_tokens, block_size, seed, wc, out_offsets, table,
+                                               out_capacity, out_hashes, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());
 }
