@@ -282,15 +282,20 @@ KV_API int kv_clip_block_lists(const int32_t *req_offsets, int32_t n_reqs, const
  * Writes the hashes, in order, to out_hashes (device uint64, 8-byte aligned, out_capacity >=
  * n_tokens / block_size) with CSR out_offsets (device int32, n_reqs + 1).  Inconsistent
  * offsets set KV_DERR_LIST and no write leaves out_hashes.  Limit: n_tokens < 2^31.
- * workspace: NULL, or device scratch of kv_block_hashes_workspace_bytes(n_tokens, block_size)
- * bytes (2 KiB per full block), 16-byte aligned; calls sharing a workspace must be ordered.
+ * workspace: NULL, or device scratch of at least 2 KiB per slot (n_tokens / block_size slots),
+ * 16-byte aligned; kv_block_hashes_workspace_bytes(n_tokens, block_size) gives the full size,
+ * 2 KiB + 4 bytes per slot rounded up to 16.  Calls sharing a workspace must be ordered.
  *  - With a workspace, every block's hash is split by a property of FNV-1a (the xor of a byte
- *    changes only the state's low byte, so the rest of a step is linear): a parallel kernel
- *    tabulates each block's token contribution for all 256 possible low bytes of the state
- *    after the parent, and one warp per request then walks its chain doing, per block, the
- *    parent's 8 byte steps, a table lookup and a multiply-add.
- *  - Without one, one thread per request runs the plain byte chain (about 8x slower for
- *    16-token blocks).  Both give the same hashes.
+ *    changes only the state's low byte, so the rest of a step is linear): each block's token
+ *    contribution is tabulated for all 256 possible low bytes of the state after the parent,
+ *    in parallel, and one warp per request then walks its chain doing, per block, the
+ *    low-byte chain of the parent's 8 bytes, a table lookup and a sum.  With the full size,
+ *    the tables and the walks run in one cooperative launch (walkers on SMs of their own read
+ *    each table once it is published) when the walk is the longer part, as for a few long
+ *    prompts; otherwise, or with a workspace of the tables alone, a table kernel runs first.
+ *    A wait that runs out (2 s) sets KV_DERR_TIMEOUT.
+ *  - Without one, one thread per request runs the plain byte chain (about 5x slower for
+ *    16-token blocks).  Every path gives the same hashes.
  */
 KV_API int kv_block_hashes_workspace_bytes(int64_t n_tokens, int32_t block_size, int64_t *bytes_out);
 KV_API int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const int32_t *tokens, int64_t n_tokens,

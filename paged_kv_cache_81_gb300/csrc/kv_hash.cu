@@ -7,16 +7,19 @@
 // followed by the block's token ids as 4 little-endian bytes each.  Only full blocks are hashed.
 //
 // FNV-1a is byte-serial and each block starts from its parent's hash, so a request's chain is
-// sequential.  One CTA first scans the full-block counts into the output CSR offsets.  Then,
-// with a workspace, two kernels split each block's hash by a property of FNV-1a: the xor of a
-// byte only changes the state's low byte c, so a step is h' = P (h + d) with d = (c ^ b) - c
+// sequential.  With a workspace, each block's hash is split by a property of FNV-1a: the xor of
+// a byte only changes the state's low byte c, so a step is h' = P (h + d) with d = (c ^ b) - c
 // in [-255, 255], and c itself evolves alone: c' = ((c ^ b) * P) mod 256.  Over a block's n
 // token bytes, from the state S reached after the parent's 8 bytes,
 //     H = P^n S + D[S mod 256],   D[c] = sum_k P^(n-k) d_k  (the d_k of the chain started at c),
-// and D depends only on the block's tokens.  The table kernel fills D for every block and all
-// 256 values of c at once, spread over the whole GPU; the walker then needs, per block, only
-// parent's 8 byte steps, one shared-memory lookup and a multiply-add.  Without a workspace one
-// thread per request runs the plain byte chain.
+// and D depends only on the block's tokens.  Tables of D for every block and all 256 values of
+// c are filled in parallel; a walk per request then needs, per block, the low-byte chain of
+// the parent's 8 bytes, one shared-memory lookup and a sum.  Two ways to run it:
+//  - tables, then the walk: a table kernel over the whole GPU (its CTA 0 also scans the
+//    full-block counts into the output offsets), then one warp per request;
+//  - both in one cooperative launch, when the walk is the longer part: walkers on SMs of their
+//    own read each table once its flag is set by the CTAs computing them.
+// Without a workspace, one CTA scans the counts and one thread per request runs the plain chain.
 #include <algorithm>
 #include <mutex>
 
@@ -25,11 +28,12 @@
 #ifndef PKV_HASH_PDL
 #define PKV_HASH_PDL 1  // 0: plain stream-ordered launches for every hash kernel
 #endif
-// The walk runs one single-warp CTA per request, and each request's chain of dependent blocks
-// sets the call's time.  Launched early (programmatic dependent launch), those few CTAs are
-// placed while the table kernel's last wave still holds the SMs, on the few with room, and the
-// walk took 182 us instead of 100 us on 8 requests of 576 blocks; launched plainly they spread
-// over idle SMs.
+// After the table kernel, the walk runs one small CTA per request, and each request's chain of
+// dependent blocks sets the call's time.  Launched early (programmatic dependent launch), an
+// earlier single-warp walk's few CTAs were placed while the table kernel's last wave still held
+// the SMs, on the few with room, and took 182 us instead of 100 us on 8 requests of 576 blocks;
+// launched plainly they spread over idle SMs.  With a ring of 66 or 98 KiB per CTA, launching
+// it early measured the same as plainly (84.3 vs 84.4 and 80.1 vs 80.3 us per call).
 #ifndef PKV_HASH_WALK_PDL
 #define PKV_HASH_WALK_PDL 0
 #endif
@@ -74,8 +78,8 @@ __device__ __forceinline__ Fnv fnv_block_start(uint64_t parent)
     return fnv_bytes<8>(Fnv{(uint32_t)kFnvBasis, (uint32_t)(kFnvBasis >> 32)}, parent);
 }
 
-// The full-block count of every request scanned into the output CSR offsets by one CTA of
-// THREADS threads (also flags offsets that do not describe n_tokens tokens).
+// The full-block count of every request scanned into CSR offsets (global or shared memory) by
+// one CTA of THREADS threads; with err, also flags offsets that do not describe n_tokens tokens.
 template <int THREADS>
 __device__ void count_blocks(const int32_t *__restrict__ off, int32_t n_reqs, int32_t n_tokens, int32_t bs,
                              int32_t *out_off, int *err)
@@ -85,7 +89,7 @@ __device__ void count_blocks(const int32_t *__restrict__ off, int32_t n_reqs, in
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         carry = 0;
-        if (off[0] != 0 || off[n_reqs] != n_tokens) pkv::set_error(err, KV_DERR_LIST);
+        if (err != nullptr && (off[0] != 0 || off[n_reqs] != n_tokens)) pkv::set_error(err, KV_DERR_LIST);
     }
     __syncthreads();
     for (int32_t base = 0; base < n_reqs; base += THREADS) {
@@ -93,7 +97,7 @@ __device__ void count_blocks(const int32_t *__restrict__ off, int32_t n_reqs, in
         int32_t cnt = 0;
         if (r < n_reqs) {
             const int32_t n = off[r + 1] - off[r];
-            if (n < 0) pkv::set_error(err, KV_DERR_LIST);
+            if (n < 0 && err != nullptr) pkv::set_error(err, KV_DERR_LIST);
             cnt = n > 0 ? n / bs : 0;
         }
         int32_t incl = cnt;
@@ -125,8 +129,8 @@ __global__ void __launch_bounds__(kScanThreads) hash_count_kernel(const int32_t 
     count_blocks<kScanThreads>(off, n_reqs, n_tokens, bs, out_off, err);
 }
 
-// Request r's span, block count and first hash index; false (and KV_DERR_LIST where the output
-// range is at fault) when r is skipped.
+// Request r's span, block count and first hash index; false (and, with err, KV_DERR_LIST where
+// the output range is at fault) when r is skipped.
 __device__ __forceinline__ bool request_blocks(const int32_t *off, int32_t r, int32_t n_tokens, int32_t bs,
                                                const int32_t *out_off, int64_t limit, int *err, int32_t *begin,
                                                int32_t *k, int64_t *at)
@@ -137,7 +141,7 @@ __device__ __forceinline__ bool request_blocks(const int32_t *off, int32_t r, in
     *k = n / bs;
     *at = out_off[r];
     if (*at < 0 || *at + *k > limit) {
-        pkv::set_error(err, KV_DERR_LIST);
+        if (err != nullptr) pkv::set_error(err, KV_DERR_LIST);
         return false;
     }
     return *k > 0;
@@ -244,17 +248,73 @@ __device__ __forceinline__ uint64_t join_weight(SplitWeight s)
 // entry x, D[(x * P) mod 256]: the entry for the state's low byte before the last multiply of
 // the parent bytes, which saves the walk that multiply.
 //
-// The table kernel: slot i, i = blockIdx.x, + gridDim.x, ...; the block (if any) that starts
-// in tokens [i * bs, (i + 1) * bs) belongs to the request holding token (i + 1) * bs - 1.
 // D = sum_k P^(n-k) d_k is a weighted sum over the block's bytes in chunks of at most
 // kTableChunk tokens, joined by Horner (D <- D * P^(chunk bytes) + chunk sum).  The weights
-// P^(M - i), M = min(n, 4 kTableChunk), are computed once per CTA into shared memory; a chunk
-// of m bytes uses the last m of them.  Per byte: a byte extract and xor, one subtraction, a
-// signed 32x32->64 multiply-add, a 32-bit multiply-add, and the chain's multiply.  Tokens are
-// read straight from global memory (the same address across the CTA), so a slot needs no
-// barrier.  When scan is set, CTA 0 first writes the output offsets.
+// P^(M - i), M = min(n, 4 kTableChunk), sit in shared memory; a chunk of m bytes uses the last m
+// of them.  Per byte: a byte extract and xor, one subtraction, a signed 32x32->64 multiply-add,
+// a 32-bit multiply-add, and the chain's multiply.  Tokens are read straight from global memory
+// (the same address across the threads of a table), so a table needs no barrier.
 constexpr int kTableChunkBytes = 4 * kTableChunk;
 
+// The weights P^(M - i), i < M, into sh_w by nthreads threads (a barrier must follow).
+__device__ __forceinline__ void fill_weights(SplitWeight *sh_w, int32_t M, int tid, int nthreads)
+{
+    // thread tid takes i = tid, tid + 256, ... (256 divides nthreads; P^-256 steps between them)
+    if (tid < kTableThreads && tid < M) {
+        uint64_t w = pow_mod_2_64(kFnvPrime, (uint64_t)(M - tid));
+        for (int32_t i = tid; i < M; i += kTableThreads) {
+            sh_w[i] = split_weight(w);  // P^(M - i)
+            w *= kPrimeInvPow256;       // P^(M - i - 256)
+        }
+    }
+    (void)nthreads;
+}
+
+// D for the block of bs tokens at tp and the starting low byte c0.
+__device__ __forceinline__ uint64_t table_entry(const int32_t *__restrict__ tp, int32_t bs, uint32_t c0,
+                                                const SplitWeight *sh_w, int32_t M)
+{
+    uint32_t c = c0;
+    uint64_t D = 0;
+    for (int32_t j0 = 0; j0 < bs; j0 += kTableChunk) {
+        const int32_t m = min(kTableChunk, bs - j0);
+        const SplitWeight *w = sh_w + (M - 4 * m);
+        int64_t acc = 0;
+        uint32_t acc_hi = 0;
+        // c keeps the product's high bits: x and c then share all but their low byte, so
+        // x - c is still the low bytes' difference, and x's low byte alone sets c's next one.
+        auto token = [&](uint32_t v, int32_t q) {
+            // a token's 4 weights are 32 contiguous bytes (w + 4q is 32-byte aligned: chunks
+            // start at a multiple of 4 weights): two 16-byte loads
+            const uint4 w01 = *reinterpret_cast<const uint4 *>(w + 4 * q);
+            const uint4 w23 = *reinterpret_cast<const uint4 *>(w + 4 * q + 2);
+            const uint32_t wl[4] = {w01.x, w01.z, w23.x, w23.z}, wh[4] = {w01.y, w01.w, w23.y, w23.w};
+#pragma unroll
+            for (int byte = 0; byte < 4; byte++) {
+                const uint32_t x = c ^ ((v >> (8 * byte)) & 0xffu);
+                const int32_t d = (int32_t)x - (int32_t)c;
+                acc += (int64_t)d * (int32_t)wl[byte];
+                acc_hi += (uint32_t)d * wh[byte];
+                c = x * 0x1b3u;
+            }
+        };
+        int32_t q = 0;
+        for (; q + kTableGroup <= m; q += kTableGroup) {
+            uint32_t v[kTableGroup];
+#pragma unroll
+            for (int g = 0; g < kTableGroup; g++) v[g] = (uint32_t)__ldg(tp + j0 + q + g);
+#pragma unroll
+            for (int g = 0; g < kTableGroup; g++) token(v[g], q + g);
+        }
+        for (; q < m; q++) token((uint32_t)__ldg(tp + j0 + q), q);
+        D = D * join_weight(w[0]) + (uint64_t)acc + ((uint64_t)acc_hi << 32);
+    }
+    return D;
+}
+
+// The table kernel: slot i, i = blockIdx.x, + gridDim.x, ...; the block (if any) that starts in
+// tokens [i * bs, (i + 1) * bs) belongs to the request holding token (i + 1) * bs - 1.  When scan
+// is set, CTA 0 first writes the output offsets.
 __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
                                                                    const int32_t *__restrict__ tokens,
                                                                    int32_t n_tokens, int32_t bs, int32_t *out_off,
@@ -269,15 +329,8 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
     const bool cached = n_reqs <= kOffCache;
     if (cached)
         for (int i = tid; i <= n_reqs; i += kTableThreads) sh_off[i] = off[i];
-    const int32_t nb = 4 * bs;  // token bytes per block
-    const int32_t M = min(nb, kTableChunkBytes);
-    if (tid < M) {
-        uint64_t w = pow_mod_2_64(kFnvPrime, (uint64_t)(M - tid));
-        for (int32_t i = tid; i < M; i += kTableThreads) {
-            sh_w[i] = split_weight(w);  // P^(M - i)
-            w *= kPrimeInvPow256;       // P^(M - i - 256)
-        }
-    }
+    const int32_t M = min(4 * bs, kTableChunkBytes);
+    fill_weights(sh_w, M, tid, kTableThreads);
     __syncthreads();
     const uint32_t c0 = ((uint32_t)tid * 0xb3u) & 0xffu;  // this thread's low byte of the state
     for (int32_t i = blockIdx.x; i < n_slots; i += gridDim.x) {
@@ -295,43 +348,7 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
         // the one token of the window at a block boundary of r: o + floor((last - o) / bs) * bs
         const int64_t first = o + (int64_t)pkv::fdiv((uint32_t)(last - o), div_bs) * bs;
         if (first + bs > o1 || first + bs > n_tokens) continue;  // no block starts here
-        const int32_t *tp = tokens + first;
-        uint32_t c = c0;
-        uint64_t D = 0;
-        for (int32_t j0 = 0; j0 < bs; j0 += kTableChunk) {
-            const int32_t m = min(kTableChunk, bs - j0);
-            const SplitWeight *w = sh_w + (M - 4 * m);
-            int64_t acc = 0;
-            uint32_t acc_hi = 0;
-            // c keeps the product's high bits: x and c then share all but their low byte, so
-            // x - c is still the low bytes' difference, and x's low byte alone sets c's next one.
-            auto token = [&](uint32_t v, int32_t q) {
-                // a token's 4 weights are 32 contiguous bytes (w + 4q is 32-byte aligned: chunks
-                // start at a multiple of 4 weights): two 16-byte loads
-                const uint4 w01 = *reinterpret_cast<const uint4 *>(w + 4 * q);
-                const uint4 w23 = *reinterpret_cast<const uint4 *>(w + 4 * q + 2);
-                const uint32_t wl[4] = {w01.x, w01.z, w23.x, w23.z}, wh[4] = {w01.y, w01.w, w23.y, w23.w};
-#pragma unroll
-                for (int byte = 0; byte < 4; byte++) {
-                    const uint32_t x = c ^ ((v >> (8 * byte)) & 0xffu);
-                    const int32_t d = (int32_t)x - (int32_t)c;
-                    acc += (int64_t)d * (int32_t)wl[byte];
-                    acc_hi += (uint32_t)d * wh[byte];
-                    c = x * 0x1b3u;
-                }
-            };
-            int32_t q = 0;
-            for (; q + kTableGroup <= m; q += kTableGroup) {
-                uint32_t v[kTableGroup];
-#pragma unroll
-                for (int g = 0; g < kTableGroup; g++) v[g] = (uint32_t)__ldg(tp + j0 + q + g);
-#pragma unroll
-                for (int g = 0; g < kTableGroup; g++) token(v[g], q + g);
-            }
-            for (; q < m; q++) token((uint32_t)__ldg(tp + j0 + q), q);
-            D = D * join_weight(w[0]) + (uint64_t)acc + ((uint64_t)acc_hi << 32);
-        }
-        table[(int64_t)i * 256 + tid] = D;
+        table[(int64_t)i * 256 + tid] = table_entry(tokens + first, bs, c0, sh_w, M);
     }
 }
 
@@ -344,6 +361,8 @@ struct WalkConsts {
     uint64_t k0;
     SplitWeight w[8];
 };
+
+constexpr unsigned long long kWaitNs = 2000000000ull;  // every wait gives up after 2 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -367,14 +386,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait (2 s of globaltimer) for the phase with the given parity; false when it ran out.
+// Bounded wait for the phase with the given parity; false when it ran out.
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = now_ns();
     while (!mbar_try_wait(bar, parity))
-        if (now_ns() - t0 > 2000000000ull) return false;
+        if (now_ns() - t0 > kWaitNs) return false;
     return true;
+}
+
+__device__ __forceinline__ int32_t ld_flag(const int32_t *p)
+{
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // One block of the walk from parent h; tab is the shared address of the block's table (2 KiB
@@ -409,92 +435,296 @@ __device__ __forceinline__ uint64_t walk_block(uint64_t h, const WalkConsts &wc,
     return (uint64_t)acc + ((uint64_t)acc_hi << 32) + t;
 }
 
-// One warp per request (one warp per CTA).  Lane 0 copies the request's tables into a ring of
-// kSegs segments of kSeg tables, one bulk copy (cp.async.bulk, completion counted on the
-// segment's mbarrier) per segment, kSegs - 1 segments ahead of the walk.  Every lane runs the
-// same chain; lane q keeps the q-th hash of a segment, and lanes 0 .. kSeg - 1 store them
-// together.  A wait that runs out (2 s) sets KV_DERR_TIMEOUT; the CTA then waits, bounded
-// again, for its copies still in flight and returns.
-__global__ void __launch_bounds__(32) hash_walk_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
-                                                       int32_t n_tokens, int32_t bs, uint64_t seed,
-                                                       const __grid_constant__ WalkConsts wc,
-                                                       const int32_t *__restrict__ out_off,
-                                                       const uint64_t *__restrict__ table, int64_t limit,
-                                                       uint64_t *__restrict__ out, int *err)
+// The walk of requests r0, r0 + r_step, ... by two warps of a CTA.  The tables of a request go
+// through a ring of kSegs segments of kSeg tables in shared memory (ring: its 2 KiB aligned
+// shared address), one bulk copy (cp.async.bulk) per segment.  Warp 1, the producer, issues the
+// copies up to kSegs segments ahead: it waits for the segment's slot to be released (mbarrier
+// empty[slot]), and with FLAGS (the tables still being written by other CTAs) until the flags of
+// all its tables are set, after which an acquire fence and a proxy fence make the tables visible
+// to the bulk copy; completion is counted on mbarrier full[slot].  Warp 0, the walker, waits
+// for full[slot], walks the segment's blocks (every lane runs the same chain, lane 0 stores each
+// hash; a full segment has no bound check per block) and releases the slot.  The fences and
+// flag polls thus stay off the walker, and both warps go through the same sequence of
+// (request, segment), numbered G across requests: slot G % kSegs, use G / kSegs.  A wait that
+// runs out (2 s) sets KV_DERR_TIMEOUT and ends that warp's walk; the producer then waits,
+// bounded again, for its copies still in flight.
+template <bool FLAGS>
+__device__ void walk_requests(int32_t r0, int32_t r_step, const int32_t *__restrict__ off, int32_t n_reqs,
+                              int32_t n_tokens, int32_t bs, uint64_t seed, const WalkConsts &wc, const int32_t *at_of,
+                              int64_t limit, const uint64_t *__restrict__ table, const int32_t *flags,
+                              uint64_t *__restrict__ out, int *err, uint32_t ring, const uint64_t *full,
+                              const uint64_t *empty)
 {
-    pkv::grid_dep_entry();  // before any global memory access
-    extern __shared__ __align__(16) uint8_t walk_smem[];
-    __shared__ __align__(8) uint64_t bar[kSegs];
-    const int lane = threadIdx.x;
-    const uint32_t ring = (smem_addr(walk_smem) + kTableBytes - 1) & ~(kTableBytes - 1);
-    if (lane == 0) {
-        for (int s = 0; s < kSegs; s++)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    uint32_t parity = 0;  // bit s: the parity of segment slot s's next phase
-    for (int32_t r = blockIdx.x; r < n_reqs; r += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    const bool producer = (threadIdx.x >> 5) == 1;
+    uint32_t G = 0;  // segments of this CTA so far
+    for (int32_t r = r0; r < n_reqs; r += r_step) {
         int32_t begin, k;
         int64_t at;
-        if (!request_blocks(off, r, n_tokens, bs, out_off, limit, err, &begin, &k, &at)) continue;
-        const uint64_t *tab = table + (int64_t)(begin / bs) * 256;
+        if (!request_blocks(off, r, n_tokens, bs, at_of, limit, producer ? nullptr : err, &begin, &k, &at)) continue;
+        const int32_t slot0 = begin / bs;
         const int32_t nseg = (k + kSeg - 1) / kSeg;
-        auto issue = [&](int32_t s) {  // segment s into its ring slot, issued by lane 0 (predicated, no branch)
-            const uint32_t slot = (uint32_t)(s % kSegs);
-            const uint32_t bytes = (uint32_t)min(kSeg, k - s * kSeg) * kTableBytes;
+        if (producer) {
+            for (int32_t s = 0; s < nseg; s++, G++) {
+                const uint32_t slot = G % kSegs, use = G / kSegs;
+                bool ok = use == 0 || __all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[slot]), (use - 1) & 1u));
+                if (ok && FLAGS) {
+                    const int32_t j = s * kSeg + lane;
+                    const bool mine = lane < kSeg && j < k;
+                    const unsigned long long t0 = now_ns();
+                    while (!__all_sync(0xffffffffu, !mine || ld_flag(flags + slot0 + j) != 0))
+                        if (__shfl_sync(0xffffffffu, now_ns() - t0 > kWaitNs, 0)) {
+                            ok = false;
+                            break;
+                        }
+                    if (ok) {
+                        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                }
+                if (!ok) {  // let the copies still in flight land before shared memory goes away
+                    if (lane == 0) pkv::set_error(err, KV_DERR_TIMEOUT);
+                    for (uint32_t g = G > kSegs ? G - kSegs : 0; g < G; g++)
+                        mbar_wait(smem_addr(&full[g % kSegs]), (g / kSegs) & 1u);
+                    return;
+                }
+                const uint32_t bytes = (uint32_t)min(kSeg, k - s * kSeg) * kTableBytes;
+                asm volatile(  // issued by lane 0 (predicated, no branch)
+                    "{\n\t.reg .pred p;\n\t"
+                    "setp.eq.u32 p, %0, 0;\n\t"
+                    "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t"
+                    "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%3], [%4], %2, [%1];\n\t"
+                    "}" ::"r"(lane),
+                    "r"(smem_addr(&full[slot])), "r"(bytes), "r"(ring + slot * (uint32_t)(kSeg * kTableBytes)),
+                    "l"(table + ((int64_t)slot0 + (int64_t)s * kSeg) * 256)
+                    : "memory");
+            }
+            continue;
+        }
+        uint64_t h = seed;
+        for (int32_t s = 0; s < nseg; s++, G++) {
+            const uint32_t slot = G % kSegs, use = G / kSegs;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&full[slot]), use & 1u))) {
+                if (lane == 0) pkv::set_error(err, KV_DERR_TIMEOUT);
+                return;
+            }
+            const uint32_t seg = ring + slot * (uint32_t)(kSeg * kTableBytes);
+            const int32_t j0 = s * kSeg;
+            if (j0 + kSeg <= k) {  // a full segment: no bound per block
+#pragma unroll
+                for (int q = 0; q < kSeg; q++) {
+                    h = walk_block(h, wc, seg + (uint32_t)q * kTableBytes);
+                    if (lane == 0) out[at + j0 + q] = h;
+                }
+            } else {
+#pragma unroll 1
+                for (int q = 0; j0 + q < k; q++) {
+                    h = walk_block(h, wc, seg + (uint32_t)q * kTableBytes);
+                    if (lane == 0) out[at + j0 + q] = h;
+                }
+            }
+            __syncwarp();  // every lane has read the segment before it is released
             asm volatile(
                 "{\n\t.reg .pred p;\n\t"
                 "setp.eq.u32 p, %0, 0;\n\t"
-                "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t"
-                "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%3], [%4], %2, [%1];\n\t}" ::"r"(
-                    lane),
-                "r"(smem_addr(&bar[slot])), "r"(bytes), "r"(ring + slot * (uint32_t)(kSeg * kTableBytes)),
-                "l"(tab + (int64_t)s * kSeg * 256)
+                "@p mbarrier.arrive.shared::cta.b64 _, [%1];\n\t}" ::"r"(lane),
+                "r"(smem_addr(&empty[slot]))
                 : "memory");
-        };
-        for (int32_t s = 0; s < min(nseg, kSegs); s++) issue(s);
-        uint64_t h = seed;
-        for (int32_t s = 0; s < nseg; s++) {
-            const uint32_t slot = (uint32_t)(s % kSegs);
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar[slot]), (parity >> slot) & 1u))) {
-                // let the copies still in flight (this one included) land before shared memory goes away
-                if (lane == 0) pkv::set_error(err, KV_DERR_TIMEOUT);
-                for (int32_t s2 = s; s2 < min(nseg, s + kSegs); s2++) {
-                    const uint32_t sl = (uint32_t)(s2 % kSegs);
-                    mbar_wait(smem_addr(&bar[sl]), (parity >> sl) & 1u);
-                    parity ^= 1u << sl;
-                }
-                return;
-            }
-            parity ^= 1u << slot;
-            const uint32_t seg = ring + slot * (uint32_t)(kSeg * kTableBytes);
-            const int32_t j0 = s * kSeg;
-            uint64_t keep = 0;
-#pragma unroll
-            for (int q = 0; q < kSeg; q++) {
-                if (j0 + q >= k) break;
-                h = walk_block(h, wc, seg + (uint32_t)q * kTableBytes);
-                if (lane == q) keep = h;
-            }
-            if (lane < kSeg && j0 + lane < k) out[at + j0 + lane] = keep;
-            __syncwarp();  // every lane has read the segment before it is refilled
-            if (s + kSegs < nseg) issue(s + kSegs);
         }
     }
+}
+
+// The ring's 2 KiB aligned shared address and its barriers' initialisation (by thread 0, then a
+// CTA barrier over the walk's two warps).
+__device__ __forceinline__ uint32_t walk_ring_setup(const uint8_t *walk_smem, uint64_t *full, uint64_t *empty)
+{
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSegs; s++) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&empty[s])) : "memory");
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    return (smem_addr(walk_smem) + kTableBytes - 1) & ~(kTableBytes - 1);
+}
+
+// The walk after the table kernel: a CTA of two warps per request.
+constexpr int kWalkThreads = 64;
+
+__global__ void __launch_bounds__(kWalkThreads) hash_walk_kernel(const int32_t *__restrict__ off, int32_t n_reqs,
+                                                                 int32_t n_tokens, int32_t bs, uint64_t seed,
+                                                                 const __grid_constant__ WalkConsts wc,
+                                                                 const int32_t *__restrict__ out_off,
+                                                                 const uint64_t *__restrict__ table, int64_t limit,
+                                                                 uint64_t *__restrict__ out, int *err)
+{
+    pkv::grid_dep_entry();  // before any global memory access
+    extern __shared__ __align__(16) uint8_t walk_smem[];
+    __shared__ __align__(8) uint64_t full[kSegs], empty[kSegs];
+    const uint32_t ring = walk_ring_setup(walk_smem, full, empty);
+    walk_requests<false>(blockIdx.x, gridDim.x, off, n_reqs, n_tokens, bs, seed, wc, out_off, limit, table, nullptr,
+                         out, err, ring, full, empty);
+}
+
+// ---- the table kernel and the walk in one cooperative launch ----
+// One CTA per SM (its shared memory holds a whole walk ring).  CTAs below n_walk walk request
+// blockIdx.x, + n_walk, ... on their own SMs (warp 0; they first scan the counts themselves, and
+// CTA 0 writes the output offsets).  The other CTAs compute tables, a group of 256 threads per
+// table, in block-position order (block 0 of every request, then block 1, ...) so the walks
+// find their tables ready; a group publishes a table's flag once it has computed its next one,
+// so the release fence finds the table's stores long done.  The flags (one int per slot, after
+// the tables in the workspace) are cleared before the launch.
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedGroups = kFusedThreads / kTableThreads;
+
+__device__ __forceinline__ void group_sync(int g)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "n"(kTableThreads) : "memory");
+}
+
+__device__ __forceinline__ void publish(int32_t *flag)
+{
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1) hash_fused_kernel(
+    const int32_t *__restrict__ off, int32_t n_reqs, const int32_t *__restrict__ tokens, int32_t n_tokens,
+    int32_t bs, pkv::FastDiv div_bs, uint64_t seed, const __grid_constant__ WalkConsts wc, int32_t *out_off,
+    uint64_t *__restrict__ table, int32_t *flags, int32_t n_walk, int64_t limit, uint64_t *__restrict__ out, int *err)
+{
+    pkv::grid_dep_entry();  // before any global memory access
+    extern __shared__ __align__(16) uint8_t walk_smem[];
+    __shared__ __align__(16) SplitWeight sh_w[kTableChunkBytes];
+    __shared__ int32_t sh_off[kOffCache + 1];
+    __shared__ __align__(8) uint64_t full[kSegs], empty[kSegs];
+    __shared__ int32_t sh_max_k;
+    const int tid = threadIdx.x;
+    if ((int32_t)blockIdx.x < n_walk) {
+        // sh_off serves as this CTA's copy of the output offsets
+        count_blocks<kFusedThreads>(off, n_reqs, n_tokens, bs, sh_off, blockIdx.x == 0 ? err : nullptr);
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int i = tid; i <= n_reqs; i += kFusedThreads) out_off[i] = sh_off[i];
+        if (tid >= kWalkThreads) return;
+        const uint32_t ring = walk_ring_setup(walk_smem, full, empty);
+        walk_requests<true>(blockIdx.x, n_walk, off, n_reqs, n_tokens, bs, seed, wc, sh_off, limit, table, flags, out,
+                            err, ring, full, empty);
+        return;
+    }
+    for (int i = tid; i <= n_reqs; i += kFusedThreads) sh_off[i] = off[i];
+    const int32_t M = min(4 * bs, kTableChunkBytes);
+    fill_weights(sh_w, M, tid, kFusedThreads);
+    if (tid == 0) sh_max_k = 0;
+    __syncthreads();
+    for (int r = tid; r < n_reqs; r += kFusedThreads) {  // the most full blocks of any request
+        const int32_t o = sh_off[r], n = sh_off[r + 1] - o;
+        if (n > 0 && o >= 0 && o + n <= n_tokens) atomicMax(&sh_max_k, (int32_t)pkv::fdiv((uint32_t)n, div_bs));
+    }
+    __syncthreads();
+    const int g = tid / kTableThreads, ti = tid % kTableThreads;
+    const uint32_t c0 = ((uint32_t)ti * 0xb3u) & 0xffu;
+    // this group's items: (block b, request r) = w, w + W, ... of b * n_reqs + r
+    const int64_t W = (int64_t)(gridDim.x - n_walk) * kFusedGroups;
+    const int64_t n_items = (int64_t)n_reqs * sh_max_k;
+    const int64_t w0 = (int64_t)(blockIdx.x - n_walk) * kFusedGroups + g;
+    int64_t b = w0 / n_reqs;
+    int32_t r = (int32_t)(w0 % n_reqs);
+    const int64_t step_b = W / n_reqs;
+    const int32_t step_r = (int32_t)(W % n_reqs);
+    int32_t prev = -1;  // the slot computed last, not yet published
+    bool first = true;
+    for (int64_t item = w0; item < n_items; item += W) {
+        const int32_t o = sh_off[r], n = sh_off[r + 1] - o;
+        const int64_t kr = (n > 0 && o >= 0 && o + n <= n_tokens) ? pkv::fdiv((uint32_t)n, div_bs) : 0;
+        if (b < kr) {
+            const int32_t slot = (int32_t)(pkv::fdiv((uint32_t)o, div_bs) + b);
+            const uint64_t D = table_entry(tokens + o + b * bs, bs, c0, sh_w, M);
+            group_sync(g);  // the group's stores of the previous table are all issued
+            if (ti == 0 && prev >= 0) publish(flags + prev);
+            table[(int64_t)slot * 256 + ti] = D;
+            prev = slot;
+            if (first) {  // the walks are waiting for the first tables: publish this one at once
+                group_sync(g);
+                if (ti == 0) publish(flags + slot);
+                prev = -1;
+                first = false;
+            }
+        }
+        b += step_b;
+        r += step_r;
+        if (r >= n_reqs) {
+            r -= n_reqs;
+            b++;
+        }
+    }
+    group_sync(g);
+    if (ti == 0 && prev >= 0) publish(flags + prev);
 }
 
 }  // namespace
 
 int pkv::preload_hash_kernels()
 {
-    return pkv::load_kernels(hash_count_kernel, hash_chain_kernel, hash_table_kernel, hash_walk_kernel);
+    return pkv::load_kernels(hash_count_kernel, hash_chain_kernel, hash_table_kernel, hash_walk_kernel,
+                             hash_fused_kernel);
 }
+
+namespace {
+
+// Workspace: the tables (2 KiB per slot), then one flag per slot for the fused launch.
+int64_t tables_bytes(int64_t n_slots) { return n_slots * (int64_t)kTableBytes; }
+int64_t fused_workspace_bytes(int64_t n_slots)
+{
+    return (tables_bytes(n_slots) + n_slots * (int64_t)sizeof(int32_t) + 15) & ~(int64_t)15;
+}
+
+// Per device, once: both walk kernels may use a whole ring of shared memory, and whether the
+// fused launch can run (cooperative launches supported, one CTA fits on an SM).
+int prepare_device(const pkv::DeviceInfo *dev, bool *fused_ok)
+{
+    static std::mutex mu;
+    static bool done[64], ok[64];
+    std::lock_guard<std::mutex> lock(mu);
+    const int d = dev->device & 63;
+    if (!done[d]) {
+        int st = pkv::cuda_status(
+            cudaFuncSetAttribute(hash_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWalkSmem));
+        if (st == KV_OK)
+            st = pkv::cuda_status(
+                cudaFuncSetAttribute(hash_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWalkSmem));
+        int coop = 0, per_sm = 0;
+        if (st == KV_OK) st = pkv::cuda_status(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev->device));
+        if (st == KV_OK)
+            st = pkv::cuda_status(
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hash_fused_kernel, kFusedThreads, kWalkSmem));
+        if (st != KV_OK) return st;
+        ok[d] = coop != 0 && per_sm >= 1;
+        done[d] = true;
+    }
+    *fused_ok = ok[d];
+    return KV_OK;
+}
+
+// Whether the fused launch pays.  Its walkers take n_reqs SMs from the tables.  On GB300 the tables
+// cost about 0.064 us x SM per token and the walk about 0.08 us per block of the longest request,
+// which holds at least n_slots / n_reqs blocks; the fused launch is taken when the tables' loss,
+// T_tables * n_reqs / (S - n_reqs), stays under half the walk:
+//     bs * 0.064 * n_reqs^2 < 0.5 * 0.08 * S * (S - n_reqs),  i.e.  8 bs n_reqs^2 < 5 S (S - n_reqs).
+// (8 prompts of 576 blocks of 16 tokens: fused; 32 requests of 64-token blocks: tables then walk.)
+bool fused_pays(int32_t bs, int32_t n_reqs, int num_sms)
+{
+    if (n_reqs > num_sms / 4) return false;
+    return 8ll * bs * n_reqs * n_reqs < 5ll * num_sms * (num_sms - n_reqs);
+}
+
+}  // namespace
 
 extern "C" int kv_block_hashes_workspace_bytes(int64_t n_tokens, int32_t block_size, int64_t *bytes_out)
 {
     if (bytes_out == nullptr || n_tokens < 0 || block_size <= 0) return KV_ERR_INVALID_ARG;
-    *bytes_out = (n_tokens / block_size) * 256 * (int64_t)sizeof(uint64_t);
+    *bytes_out = fused_workspace_bytes(n_tokens / block_size);
     return KV_OK;
 }
 
@@ -510,21 +740,26 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
     if (out_capacity < n_tokens / block_size) return KV_ERR_RANGE;
     if (out_capacity > 0 && out_hashes == nullptr) return KV_ERR_INVALID_ARG;
     if (((uintptr_t)out_hashes & 7u) != 0) return KV_ERR_ALIGN;
-    int64_t need = 0;
-    kv_block_hashes_workspace_bytes(n_tokens, block_size, &need);
+    const int32_t n_slots = (int32_t)(n_tokens / block_size);  // out_capacity >= n_slots (checked above)
     if (workspace != nullptr) {
         if (!pkv::aligned16(workspace)) return KV_ERR_ALIGN;
-        if (workspace_bytes < need) return KV_ERR_RANGE;
+        if (workspace_bytes < tables_bytes(n_slots)) return KV_ERR_RANGE;
     }
     const pkv::DeviceInfo *dev = pkv::current_device();
     if (dev == nullptr) return KV_ERR_CUDA;
     const cudaStream_t s = (cudaStream_t)stream;
     if (n_reqs == 0) return pkv::cuda_status(cudaMemsetAsync(out_offsets, 0, sizeof(int32_t), s));
-    const int32_t n_slots = (int32_t)(n_tokens / block_size);  // out_capacity >= n_slots (checked above)
     const bool table_path = workspace != nullptr && n_slots > 0;
-    const bool fused_scan = table_path && n_reqs <= kFusedScanMaxReqs;
+    bool fused_ok = false;
     int st = KV_OK;
-    if (!fused_scan) {
+    if (table_path) {
+        st = prepare_device(dev, &fused_ok);
+        if (st != KV_OK) return st;
+    }
+    const bool fused = table_path && fused_ok && workspace_bytes >= fused_workspace_bytes(n_slots) &&
+                       n_reqs <= kOffCache && fused_pays(block_size, n_reqs, dev->num_sms);
+    const bool fused_scan = table_path && n_reqs <= kFusedScanMaxReqs;  // the two-kernel path's table CTA 0 scans
+    if (!table_path || !fused_scan) {
         pkv::launch<kHashPdl>(hash_count_kernel, 1, kScanThreads, 0, s, tok_offsets, n_reqs, (int32_t)n_tokens,
                               block_size, out_offsets, dev->err_word);
         st = pkv::cuda_status(cudaGetLastError());
@@ -539,29 +774,41 @@ extern "C" int kv_block_hashes(const int32_t *tok_offsets, int32_t n_reqs, const
     }
     if (n_slots == 0) return KV_OK;
     uint64_t *table = reinterpret_cast<uint64_t *>(workspace);
-    const int table_blocks = std::min(n_slots, dev->num_sms * 8);
-    pkv::launch<kHashPdl>(hash_table_kernel, table_blocks, kTableThreads, 0, s, tok_offsets, n_reqs, tokens,
-                          (int32_t)n_tokens, block_size, out_offsets, table, n_slots, pkv::make_fastdiv((uint32_t)block_size),
-                          fused_scan, dev->err_word);
-    st = pkv::cuda_status(cudaGetLastError());
-    if (st != KV_OK) return st;
+    const pkv::FastDiv div_bs = pkv::make_fastdiv((uint32_t)block_size);
     WalkConsts wc{};
     const uint64_t n8 = 4ull * (uint64_t)block_size + 8;  // bytes hashed per block
     wc.k0 = pow_mod_2_64(kFnvPrime, n8) * kFnvBasis;
     for (int k = 0; k < 8; k++) wc.w[k] = split_weight(pow_mod_2_64(kFnvPrime, n8 - (uint64_t)k));
-    static std::mutex mu;
-    static bool configured[64];
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (kWalkSmem > 48 * 1024 && !configured[dev->device & 63]) {
-            st = pkv::cuda_status(
-                cudaFuncSetAttribute(hash_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWalkSmem));
-            if (st != KV_OK) return st;
-            configured[dev->device & 63] = true;
-        }
+    if (fused) {
+        int32_t *flags = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(workspace) + tables_bytes(n_slots));
+        st = pkv::cuda_status(cudaMemsetAsync(flags, 0, (size_t)n_slots * sizeof(int32_t), s));
+        if (st != KV_OK) return st;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)dev->num_sms);
+        cfg.blockDim = dim3(kFusedThreads);
+        cfg.dynamicSmemBytes = kWalkSmem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, hash_fused_kernel, tok_offsets, n_reqs, tokens,
+                                                 (int32_t)n_tokens, block_size, div_bs, seed, wc, out_offsets, table,
+                                                 flags, n_reqs, out_capacity, out_hashes, dev->err_word);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return pkv::cuda_status(e);
+        // not all SMs are free (another context holds some): tables, then the walk (fused implies
+        // n_reqs <= kFusedScanMaxReqs, so the table kernel writes the output offsets)
+        (void)cudaGetLastError();
     }
+    const int table_blocks = std::min(n_slots, dev->num_sms * 8);
+    pkv::launch<kHashPdl>(hash_table_kernel, table_blocks, kTableThreads, 0, s, tok_offsets, n_reqs, tokens,
+                          (int32_t)n_tokens, block_size, out_offsets, table, n_slots, div_bs, fused_scan,
+                          dev->err_word);
+    st = pkv::cuda_status(cudaGetLastError());
+    if (st != KV_OK) return st;
     const int walk_blocks = std::min(n_reqs, dev->num_sms * 16);
-    pkv::launch<kHashPdl && PKV_HASH_WALK_PDL>(hash_walk_kernel, walk_blocks, 32, kWalkSmem, s, tok_offsets, n_reqs,
+    pkv::launch<kHashPdl && PKV_HASH_WALK_PDL>(hash_walk_kernel, walk_blocks, kWalkThreads, kWalkSmem, s, tok_offsets, n_reqs,
                                                (int32_t)n_tokens, block_size, seed, wc, out_offsets, table,
                                                out_capacity, out_hashes, dev->err_word);
     return pkv::cuda_status(cudaGetLastError());

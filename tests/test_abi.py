@@ -147,7 +147,9 @@ int main() {
 def test_hash_workspace_size(lib):
     out = ctypes.c_int64(-1)
     assert lib.kv_block_hashes_workspace_bytes(73728, 16, ctypes.byref(out)) == K.KV_OK
-    assert out.value == 4608 * 256 * 8  # one 256-entry table of 8-byte sums per full block
+    assert out.value == 4608 * (256 * 8 + 4)  # per slot: a 256-entry table of 8-byte sums and a flag
+    assert lib.kv_block_hashes_workspace_bytes(48, 16, ctypes.byref(out)) == K.KV_OK
+    assert out.value == 3 * 2052 + 4  # rounded up to a multiple of 16
     assert lib.kv_block_hashes_workspace_bytes(15, 16, ctypes.byref(out)) == K.KV_OK and out.value == 0
     assert lib.kv_block_hashes_workspace_bytes(16, 0, ctypes.byref(out)) == K.KV_ERR_INVALID_ARG
     assert lib.kv_block_hashes_workspace_bytes(-1, 16, ctypes.byref(out)) == K.KV_ERR_INVALID_ARG

@@ -26,12 +26,23 @@ def _lib():
     K.load()
 
 
-PATHS = ["table", "chain"]
+# "table": the full workspace (tables and walk in one cooperative launch when the walk is the
+# longer part, else a table kernel first); "two": a workspace of the tables alone (always a table
+# kernel, then the walk); "chain": no workspace (the plain byte chain).
+PATHS = ["table", "two", "chain"]
+
+
+def _workspace(path, n_tokens, bs):
+    if path == "chain":
+        return None
+    if path == "table":
+        return "auto"
+    return torch.empty(max(16, (n_tokens // bs) * 2048), dtype=torch.uint8, device="cuda")
 
 
 def _gpu(off, toks, bs, seed, path="table"):
     o, h = K.kv_block_hashes(torch.from_numpy(off).cuda(), torch.from_numpy(toks).cuda(), bs, seed,
-                             workspace="auto" if path == "table" else None)
+                             workspace=_workspace(path, toks.shape[0], bs))
     o = o.cpu().numpy()
     return o, h[:o[-1]].cpu().numpy().view(np.uint64)
 
@@ -84,18 +95,49 @@ def test_workspace_checked():
     off = torch.tensor([0, 32], dtype=torch.int32, device="cuda")
     toks = torch.arange(32, dtype=torch.int32, device="cuda")
     need = K.kv_block_hashes_workspace_bytes(32, 4)
-    assert need == 8 * 256 * 8
-    with pytest.raises(RuntimeError):
-        K.kv_block_hashes(off, toks, 4, 1, workspace=torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
+    assert need == 8 * (256 * 8 + 4)  # 16416: tables and flags, a multiple of 16
+    want_o, want = oracle.block_hashes(np.array([0, 32], np.int32), np.arange(32, dtype=np.int32), 4, 1)
+    for size in (need, 8 * 2048):  # the full size, and the tables alone
+        o, h = K.kv_block_hashes(off, toks, 4, 1, workspace=torch.empty(size, dtype=torch.uint8, device="cuda"))
+        np.testing.assert_array_equal(h.cpu().numpy().view(np.uint64), want)
+    with pytest.raises(RuntimeError):  # smaller than the tables
+        K.kv_block_hashes(off, toks, 4, 1, workspace=torch.empty(8 * 2048 - 16, dtype=torch.uint8, device="cuda"))
     with pytest.raises(RuntimeError):  # not 16-byte aligned
         K.kv_block_hashes(off, toks, 4, 1, workspace=torch.empty(need + 16, dtype=torch.uint8, device="cuda")[8:])
+    assert K.kv_get_last_error() == 0
+
+
+@pytest.mark.parametrize("bs", [1, 3, 16, 64, 600])
+@pytest.mark.parametrize("n_reqs", [1, 2, 5, 8, 30])
+def test_few_long_requests_every_path(bs, n_reqs):
+    """Few requests of many blocks, the case the cooperative launch serves (here: every case with
+    one or two requests, up to 8 requests of blocks up to 64 tokens, 30 requests of blocks up to
+    3 tokens; the others run the table kernel first), lengths with partial last blocks, an empty
+    request and a shared prefix; every path against the oracle, twice on one reused workspace."""
+    rng = np.random.default_rng(1000 * bs + n_reqs)
+    lens = rng.integers(0, 120 * bs if bs < 100 else 12 * bs, size=n_reqs)
+    if n_reqs > 2:
+        lens[1] = 0
+    toks = [rng.integers(-2 ** 31, 2 ** 31, size=int(n), dtype=np.int64).astype(np.int32) for n in lens]
+    if n_reqs > 4 and len(toks[3]) <= len(toks[4]):
+        toks[3] = toks[4][: len(toks[3])].copy()
+    off, flat = W.csr(toks)
+    want_o, want = oracle.block_hashes(off, flat, bs, 7)
+    ws = torch.empty(max(16, K.kv_block_hashes_workspace_bytes(flat.shape[0], bs)), dtype=torch.uint8, device="cuda")
+    for path in PATHS:
+        for _ in range(2):
+            o, h = K.kv_block_hashes(torch.from_numpy(off).cuda(), torch.from_numpy(flat).cuda(), bs, 7,
+                                     workspace=ws if path == "table" else _workspace(path, flat.shape[0], bs))
+            np.testing.assert_array_equal(o.cpu().numpy(), want_o)
+            np.testing.assert_array_equal(h[: int(want_o[-1])].cpu().numpy().view(np.uint64), want, err_msg=path)
+    assert K.kv_get_last_error() == 0
 
 
 @pytest.mark.parametrize("path", PATHS)
 def test_inconsistent_offsets_flagged(path):
     off = torch.tensor([0, 40, 20, 60], dtype=torch.int32, device="cuda")
     toks = torch.arange(60, dtype=torch.int32, device="cuda")
-    o, h = K.kv_block_hashes(off, toks, 4, 1, workspace="auto" if path == "table" else None)
+    o, h = K.kv_block_hashes(off, toks, 4, 1, workspace=_workspace(path, 60, 4))
     torch.cuda.synchronize()
     assert K.kv_get_last_error(clear=True) & K.KV_DERR_LIST
     assert h.shape[0] == 15  # capacity; the kernel bounds every write
