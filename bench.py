@@ -48,7 +48,8 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth (context; the roofline
 PG_TIMEOUT_S = 300  # process-group timeout under torchrun
 KERNEL_NAMES = ("slot_mapping", "reshape_and_cache", "build_xfer_list", "pack", "unpack")
 COPY_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_copy.cu", "paged_kv_cache_81_gb300/csrc/kv_copy.cuh",
-                "paged_kv_cache_81_gb300/csrc/kv_bulk.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
+                "paged_kv_cache_81_gb300/csrc/kv_bulk.cu", "paged_kv_cache_81_gb300/csrc/kv_async.cuh",
+                "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
 WRITE_SOURCES = ("paged_kv_cache_81_gb300/csrc/kv_write.cu", "paged_kv_cache_81_gb300/csrc/kv_common.cuh")
 # the sources whose change makes a kernel's DRAM-traffic record stale
 KERNEL_SOURCES = {"pack": COPY_SOURCES, "unpack": COPY_SOURCES, "reshape_and_cache": WRITE_SOURCES}

@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "kv_async.cuh"
 #include "kv_copy.cuh"
 
 #ifndef PKV_BULK_STAGE_BYTES
@@ -54,7 +55,6 @@ constexpr uint32_t kStage = PKV_BULK_STAGE_BYTES;  // bytes per slot (multiple o
 constexpr int kSlots = PKV_BULK_SLOTS;
 constexpr int kPipes = PKV_BULK_PIPES;  // warps (pipes) per CTA
 constexpr int kBatch = 32;             // run records fetched per warp round
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int64_t kTailDiv = PKV_BULK_TAIL_DIV;
 constexpr int kTailItemsPerPipe = PKV_BULK_TAIL_ITEMS;
 constexpr int kMaxTailCtasPerResident = 8;  // more tail chunks than this are strided over
@@ -70,47 +70,10 @@ struct PipeState {  // per pipe, in shared memory after the slot data
 
 constexpr size_t kSmemBytes = (size_t)kPipes * kSlots * kStage + (size_t)kPipes * sizeof(PipeState);
 
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long now_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity; false after kWaitLimitNs.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = now_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (now_ns() - t0 > kWaitLimitNs) return false;
-    return true;
-}
+using pkv::mbar_arrive_expect_tx;
+using pkv::mbar_init;
+using pkv::mbar_wait;
+using pkv::smem_addr;
 
 #ifndef PKV_BULK_EVICT_FIRST
 #define PKV_BULK_EVICT_FIRST 0  // L2 evict-first policy on: 0 none, 1 all bulk copies, 2 unpack's stores, 3 all stores, 4 all loads

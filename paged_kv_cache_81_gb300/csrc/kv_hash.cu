@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "kv_async.cuh"
 #include "kv_common.cuh"
 
 #ifndef PKV_HASH_PDL
@@ -362,39 +363,11 @@ struct WalkConsts {
     SplitWeight w[8];
 };
 
-constexpr unsigned long long kWaitNs = 2000000000ull;  // every wait gives up after 2 s
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long now_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity; false when it ran out.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = now_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (now_ns() - t0 > kWaitNs) return false;
-    return true;
-}
+using pkv::kWaitLimitNs;
+using pkv::mbar_init;
+using pkv::mbar_wait;
+using pkv::now_ns;
+using pkv::smem_addr;
 
 __device__ __forceinline__ int32_t ld_flag(const int32_t *p)
 {
@@ -473,7 +446,7 @@ __device__ void walk_requests(int32_t r0, int32_t r_step, const int32_t *__restr
                     const bool mine = lane < kSeg && j < k;
                     const unsigned long long t0 = now_ns();
                     while (!__all_sync(0xffffffffu, !mine || ld_flag(flags + slot0 + j) != 0))
-                        if (__shfl_sync(0xffffffffu, now_ns() - t0 > kWaitNs, 0)) {
+                        if (__shfl_sync(0xffffffffu, now_ns() - t0 > kWaitLimitNs, 0)) {
                             ok = false;
                             break;
                         }
@@ -540,8 +513,8 @@ __device__ __forceinline__ uint32_t walk_ring_setup(const uint8_t *walk_smem, ui
 {
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSegs; s++) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&empty[s])) : "memory");
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }

@@ -141,3 +141,40 @@ def test_inconsistent_offsets_flagged(path):
     torch.cuda.synchronize()
     assert K.kv_get_last_error(clear=True) & K.KV_DERR_LIST
     assert h.shape[0] == 15  # capacity; the kernel bounds every write
+
+
+@pytest.mark.parametrize("path", ["table", "two"])
+def test_hashes_replayed_from_a_cuda_graph(path):
+    """Both workspace paths captured in a CUDA graph (with the full workspace this batch of four
+    requests takes the cooperative launch: a memset of the flags, then the fused kernel) and
+    replayed after new token values are written in place, each replay against the oracle."""
+    rng = np.random.default_rng(99)
+    bs, lens = 8, [600, 1000, 37, 800]  # 75, 125, 4 and 100 full blocks
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    n = int(off[-1])
+    off_d = torch.from_numpy(off).cuda()
+    toks_d = torch.empty(n, dtype=torch.int32, device="cuda")
+    out_o = torch.empty_like(off_d)
+    out_h = torch.empty(n // bs, dtype=torch.int64, device="cuda")
+    ws = _workspace(path, n, bs)
+    if ws == "auto":
+        ws = torch.empty(K.kv_block_hashes_workspace_bytes(n, bs), dtype=torch.uint8, device="cuda")
+    toks_d.copy_(torch.from_numpy(rng.integers(-2 ** 31, 2 ** 31, size=n, dtype=np.int64).astype(np.int32)))
+    K.kv_block_hashes(off_d, toks_d, bs, 5, out_o, out_h, workspace=ws)  # eager first: per-device set-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        K.kv_block_hashes(off_d, toks_d, bs, 5, out_o, out_h, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for rep in range(3):
+        flat = rng.integers(-2 ** 31, 2 ** 31, size=n, dtype=np.int64).astype(np.int32)
+        toks_d.copy_(torch.from_numpy(flat))
+        g.replay()
+        torch.cuda.synchronize()
+        want_o, want = oracle.block_hashes(off, flat, bs, 5)
+        np.testing.assert_array_equal(out_o.cpu().numpy(), want_o)
+        np.testing.assert_array_equal(out_h[: int(want_o[-1])].cpu().numpy().view(np.uint64), want,
+                                      err_msg=f"{path} replay {rep}")
+    assert K.kv_get_last_error() == 0
