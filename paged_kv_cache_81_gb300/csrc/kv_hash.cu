@@ -16,7 +16,8 @@
 // c are filled in parallel; a walk per request then needs, per block, the low-byte chain of
 // the parent's 8 bytes, one shared-memory lookup and a sum.  Two ways to run it:
 //  - tables, then the walk: a table kernel over the whole GPU (its CTA 0 also scans the
-//    full-block counts into the output offsets), then one warp per request;
+//    full-block counts into the output offsets), then per request a CTA whose producer warp
+//    copies the tables into a shared-memory ring and whose walker warp runs the chain;
 //  - both in one cooperative launch, when the walk is the longer part: walkers on SMs of their
 //    own read each table once its flag is set by the CTAs computing them.
 // Without a workspace, one CTA scans the counts and one thread per request runs the plain chain.
@@ -50,7 +51,7 @@ static_assert(kFnvPrime == (1ull << 40) + 0x1b3u, "fnv_step multiplies by 2^40 +
 // FNV-1a state as two 32-bit halves.  One step h = (h ^ byte) * P with P = 2^40 + 0x1b3:
 // modulo 2^64, h * 2^40 only moves the low half up by 8 bits into the high half, and h * 0x1b3
 // is one 32x32->64 product of the low half plus a 32-bit product of the high half.  The low
-// half's chain (xor, one wide multiply) is the critical path of the whole hash.
+// half's chain (xor, one wide multiply) is the critical path of the plain chain.
 struct Fnv {
     uint32_t lo, hi;
 };
@@ -257,10 +258,10 @@ __device__ __forceinline__ uint64_t join_weight(SplitWeight s)
 // (the same address across the threads of a table), so a table needs no barrier.
 constexpr int kTableChunkBytes = 4 * kTableChunk;
 
-// The weights P^(M - i), i < M, into sh_w by nthreads threads (a barrier must follow).
-__device__ __forceinline__ void fill_weights(SplitWeight *sh_w, int32_t M, int tid, int nthreads)
+// The weights P^(M - i), i < M, into sh_w by the CTA's first 256 threads (a barrier must follow):
+// thread tid takes i = tid, tid + 256, ..., stepping by P^-256.
+__device__ __forceinline__ void fill_weights(SplitWeight *sh_w, int32_t M, int tid)
 {
-    // thread tid takes i = tid, tid + 256, ... (256 divides nthreads; P^-256 steps between them)
     if (tid < kTableThreads && tid < M) {
         uint64_t w = pow_mod_2_64(kFnvPrime, (uint64_t)(M - tid));
         for (int32_t i = tid; i < M; i += kTableThreads) {
@@ -268,7 +269,6 @@ __device__ __forceinline__ void fill_weights(SplitWeight *sh_w, int32_t M, int t
             w *= kPrimeInvPow256;       // P^(M - i - 256)
         }
     }
-    (void)nthreads;
 }
 
 // D for the block of bs tokens at tp and the starting low byte c0.
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kTableThreads) hash_table_kernel(const int32_t
     if (cached)
         for (int i = tid; i <= n_reqs; i += kTableThreads) sh_off[i] = off[i];
     const int32_t M = min(4 * bs, kTableChunkBytes);
-    fill_weights(sh_w, M, tid, kTableThreads);
+    fill_weights(sh_w, M, tid);
     __syncthreads();
     const uint32_t c0 = ((uint32_t)tid * 0xb3u) & 0xffu;  // this thread's low byte of the state
     for (int32_t i = blockIdx.x; i < n_slots; i += gridDim.x) {
@@ -542,8 +542,8 @@ __global__ void __launch_bounds__(kWalkThreads) hash_walk_kernel(const int32_t *
 
 // ---- the table kernel and the walk in one cooperative launch ----
 // One CTA per SM (its shared memory holds a whole walk ring).  CTAs below n_walk walk request
-// blockIdx.x, + n_walk, ... on their own SMs (warp 0; they first scan the counts themselves, and
-// CTA 0 writes the output offsets).  The other CTAs compute tables, a group of 256 threads per
+// blockIdx.x, + n_walk, ... on their own SMs with a walker and a producer warp (they first scan
+// the counts themselves, and CTA 0 writes the output offsets).  The other CTAs compute tables, a group of 256 threads per
 // table, in block-position order (block 0 of every request, then block 1, ...) so the walks
 // find their tables ready; a group publishes a table's flag once it has computed its next one,
 // so the release fence finds the table's stores long done.  The flags (one int per slot, after
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) hash_fused_kernel(
     }
     for (int i = tid; i <= n_reqs; i += kFusedThreads) sh_off[i] = off[i];
     const int32_t M = min(4 * bs, kTableChunkBytes);
-    fill_weights(sh_w, M, tid, kFusedThreads);
+    fill_weights(sh_w, M, tid);
     if (tid == 0) sh_max_k = 0;
     __syncthreads();
     for (int r = tid; r < n_reqs; r += kFusedThreads) {  // the most full blocks of any request
