@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kChainThreads) hash_chain_kernel(const int32_t
 // ---- with a workspace: tables of D, then the walk ----
 constexpr int kTableThreads = 256;  // one thread per table entry
 constexpr int kTableChunk = 512;    // tokens per Horner chunk
-constexpr int kTableGroup = 16;     // token loads issued ahead of their bytes
+constexpr int kTableUnits = 5;      // 3-token units whose loads are issued ahead of their bytes
 constexpr int kOffCache = 1024;     // request offsets a table CTA keeps in shared memory
 constexpr int kFusedScanMaxReqs = 4096;  // up to this many requests, table CTA 0 also scans the counts
 constexpr uint32_t kTableBytes = 256 * sizeof(uint64_t);
@@ -253,9 +253,10 @@ __device__ __forceinline__ uint64_t join_weight(SplitWeight s)
 // D = sum_k P^(n-k) d_k is a weighted sum over the block's bytes in chunks of at most
 // kTableChunk tokens, joined by Horner (D <- D * P^(chunk bytes) + chunk sum).  The weights
 // P^(M - i), M = min(n, 4 kTableChunk), sit in shared memory; a chunk of m bytes uses the last m
-// of them.  Per byte: a byte extract and xor, one subtraction, a signed 32x32->64 multiply-add,
-// a 32-bit multiply-add, and the chain's multiply.  Tokens are read straight from global memory
-// (the same address across the threads of a table), so a table needs no barrier.
+// of them.  Per byte: a byte extract and xor and the chain's multiply; per three bytes, two
+// 32-bit multiply-adds that give the group's sum from chain values, and the group's 64-bit
+// multiply-add (a signed 32x32->64 and two 32-bit multiply-adds).  Tokens are read straight from
+// global memory (the same address across the threads of a table), so a table needs no barrier.
 constexpr int kTableChunkBytes = 4 * kTableChunk;
 
 // The weights P^(M - i), i < M, into sh_w by the CTA's first 256 threads (a barrier must follow):
@@ -284,6 +285,7 @@ __device__ __forceinline__ uint64_t table_entry(const int32_t *__restrict__ tp, 
         uint32_t acc_hi = 0;
         // c keeps the product's high bits: x and c then share all but their low byte, so
         // x - c is still the low bytes' difference, and x's low byte alone sets c's next one.
+        // One token at a time (the last bs mod 3 tokens of a chunk):
         auto token = [&](uint32_t v, int32_t q) {
             // a token's 4 weights are 32 contiguous bytes (w + 4q is 32-byte aligned: chunks
             // start at a multiple of 4 weights): two 16-byte loads
@@ -299,14 +301,42 @@ __device__ __forceinline__ uint64_t table_entry(const int32_t *__restrict__ tp, 
                 c = x * 0x1b3u;
             }
         };
+        // Three tokens (12 bytes) at a time, their bytes in groups of three sharing the last
+        // byte's weight: W_j d_j + W_(j+1) d_(j+1) + W_(j+2) d_(j+2) = W_(j+2) v with
+        // v = P^2 d_j + P d_(j+1) + d_(j+2), and modulo 2^64, P^2 = 870 * 2^40 + 189225, so
+        // v = L + 2^40 Hh with L = 189225 d_j + 435 d_(j+1) + d_(j+2) (|L| < 2^26) and
+        // Hh = 870 d_j + d_(j+1).  The chain keeps c' = 435 x exactly (mod 2^32), so these sums
+        // telescope to chain values: L = x_(j+2) - 435^2 c_j and Hh = x_(j+1) + c_(j+1) - 870 c_j
+        // (mod 2^32; L read as signed is exact).  One 64-bit multiply-add per three bytes.
+        auto tokens3 = [&](uint32_t v0, uint32_t v1, uint32_t v2, int32_t q3) {
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                uint32_t cs[3], xs[3];
+#pragma unroll
+                for (int j = 0; j < 3; j++) {
+                    const int i = 3 * g + j;
+                    const uint32_t v = i < 4 ? v0 : (i < 8 ? v1 : v2);
+                    cs[j] = c;
+                    xs[j] = c ^ ((v >> (8 * (i & 3))) & 0xffu);
+                    c = xs[j] * 0x1b3u;
+                }
+                const int32_t L = (int32_t)(xs[2] - 189225u * cs[0]);
+                const uint32_t Hh = xs[1] + cs[1] - 870u * cs[0];
+                const SplitWeight wt = w[4 * q3 + 3 * g + 2];
+                acc += (int64_t)L * wt.lo_s;
+                acc_hi += (uint32_t)L * wt.hi + ((Hh * (uint32_t)wt.lo_s) << 8);
+            }
+        };
         int32_t q = 0;
-        for (; q + kTableGroup <= m; q += kTableGroup) {
-            uint32_t v[kTableGroup];
+        for (; q + 3 * kTableUnits <= m; q += 3 * kTableUnits) {
+            uint32_t v[3 * kTableUnits];
 #pragma unroll
-            for (int g = 0; g < kTableGroup; g++) v[g] = (uint32_t)__ldg(tp + j0 + q + g);
+            for (int g = 0; g < 3 * kTableUnits; g++) v[g] = (uint32_t)__ldg(tp + j0 + q + g);
 #pragma unroll
-            for (int g = 0; g < kTableGroup; g++) token(v[g], q + g);
+            for (int u = 0; u < kTableUnits; u++) tokens3(v[3 * u], v[3 * u + 1], v[3 * u + 2], q + 3 * u);
         }
+        for (; q + 3 <= m; q += 3)
+            tokens3((uint32_t)__ldg(tp + j0 + q), (uint32_t)__ldg(tp + j0 + q + 1), (uint32_t)__ldg(tp + j0 + q + 2), q);
         for (; q < m; q++) token((uint32_t)__ldg(tp + j0 + q), q);
         D = D * join_weight(w[0]) + (uint64_t)acc + ((uint64_t)acc_hi << 32);
     }
