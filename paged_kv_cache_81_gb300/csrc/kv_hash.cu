@@ -98,9 +98,9 @@ __device__ void count_blocks(const int32_t *__restrict__ off, int32_t n_reqs, in
         const int32_t r = base + tid;
         int32_t cnt = 0;
         if (r < n_reqs) {
-            const int32_t n = off[r + 1] - off[r];
+            const int64_t n = (int64_t)off[r + 1] - off[r];  // 64-bit: offsets may be anything
             if (n < 0 && err != nullptr) pkv::set_error(err, KV_DERR_LIST);
-            cnt = n > 0 ? n / bs : 0;
+            cnt = n > 0 ? (int32_t)(n / bs) : 0;
         }
         int32_t incl = cnt;
 #pragma unroll
@@ -138,9 +138,9 @@ __device__ __forceinline__ bool request_blocks(const int32_t *off, int32_t r, in
                                                int32_t *k, int64_t *at)
 {
     *begin = off[r];
-    const int32_t n = off[r + 1] - *begin;
+    const int64_t n = (int64_t)off[r + 1] - *begin;  // 64-bit: offsets may be anything
     if (n <= 0 || *begin < 0 || *begin + n > n_tokens) return false;
-    *k = n / bs;
+    *k = (int32_t)(n / bs);
     *at = out_off[r];
     if (*at < 0 || *at + *k > limit) {
         if (err != nullptr) pkv::set_error(err, KV_DERR_LIST);
@@ -622,7 +622,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) hash_fused_kernel(
     if (tid == 0) sh_max_k = 0;
     __syncthreads();
     for (int r = tid; r < n_reqs; r += kFusedThreads) {  // the most full blocks of any request
-        const int32_t o = sh_off[r], n = sh_off[r + 1] - o;
+        const int32_t o = sh_off[r];
+        const int64_t n = (int64_t)sh_off[r + 1] - o;  // the same test as the walks' request_blocks
         if (n > 0 && o >= 0 && o + n <= n_tokens) atomicMax(&sh_max_k, (int32_t)pkv::fdiv((uint32_t)n, div_bs));
     }
     __syncthreads();
@@ -639,7 +640,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) hash_fused_kernel(
     int32_t prev = -1;  // the slot computed last, not yet published
     bool first = true;
     for (int64_t item = w0; item < n_items; item += W) {
-        const int32_t o = sh_off[r], n = sh_off[r + 1] - o;
+        const int32_t o = sh_off[r];
+        const int64_t n = (int64_t)sh_off[r + 1] - o;
         const int64_t kr = (n > 0 && o >= 0 && o + n <= n_tokens) ? pkv::fdiv((uint32_t)n, div_bs) : 0;
         if (b < kr) {
             const int32_t slot = (int32_t)(pkv::fdiv((uint32_t)o, div_bs) + b);
