@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kPipes * 32, 1) bulk_copy_kernel(const __grid_
                         cached_req = r;
                         s0 = p.src_req_offsets[r];
                         d0 = p.dst_req_offsets[r];
-                        dn = p.dst_req_offsets[r + 1] - d0;
+                        dn = (int32_t)max((int64_t)-1, min((int64_t)INT32_MAX, (int64_t)p.dst_req_offsets[r + 1] - d0));
                     }
                     if (run.stage_block < s0 || dn < 0 || d0 < 0) {  // offsets that do not match the runs
                         pkv::set_error(p.err, KV_DERR_DST_TABLE);

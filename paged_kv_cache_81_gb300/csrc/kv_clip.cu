@@ -47,12 +47,13 @@ __global__ void __launch_bounds__(kScanThreads) clip_count_kernel(const int32_t 
         int32_t cnt = 0;
         if (r < n_reqs) {
             int64_t n = n_tokens[r];
-            int32_t len = off[r + 1] - off[r];
-            if (n < 0 || len < 0) {
+            int64_t len64 = (int64_t)off[r + 1] - off[r];  // 64-bit: offsets may be anything
+            if (n < 0 || len64 < 0) {
                 pkv::set_error(err, KV_DERR_LIST);
                 n = n < 0 ? 0 : n;
-                len = len < 0 ? 0 : len;
+                len64 = len64 < 0 ? 0 : len64;
             }
+            const int32_t len = (int32_t)(len64 > INT32_MAX ? INT32_MAX : len64);
             int32_t f, e;
             kept_range(n, window, bs, len, &f, &e);
             cnt = e - f;
@@ -94,9 +95,10 @@ __global__ void __launch_bounds__(256) clip_copy_kernel(const int32_t *__restric
             else hi = mid - 1;
         }
         const int32_t r = lo;
-        const int32_t q = i - off[r];
-        const int32_t len = off[r + 1] - off[r];
-        if (q < 0 || len <= 0) continue;
+        const int64_t q = (int64_t)i - off[r];
+        const int64_t len64 = (int64_t)off[r + 1] - off[r];  // 64-bit: offsets may be anything
+        if (q < 0 || len64 <= 0) continue;
+        const int32_t len = (int32_t)(len64 > INT32_MAX ? INT32_MAX : len64);
         const int64_t n = n_tokens[r] < 0 ? 0 : n_tokens[r];
         int32_t f, e;
         kept_range(n, window, bs, len, &f, &e);

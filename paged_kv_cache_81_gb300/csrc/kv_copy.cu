@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, MODE >= pkv::ROWS ? PKV_ROWS_MIN_CTA
             }
             const int32_t s0 = p.src_req_offsets[r];
             const int32_t d0 = p.dst_req_offsets[r];
-            dn = p.dst_req_offsets[r + 1] - d0;
+            dn = (int32_t)max((int64_t)-1, min((int64_t)INT32_MAX, (int64_t)p.dst_req_offsets[r + 1] - d0));
             if (run.stage_block < s0 || dn < 0 || d0 < 0) {  // offsets that do not match the runs
                 if (first_piece && lane == 0) pkv::set_error(p.err, KV_DERR_DST_TABLE);
                 continue;
