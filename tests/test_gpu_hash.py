@@ -178,3 +178,23 @@ def test_hashes_replayed_from_a_cuda_graph(path):
         np.testing.assert_array_equal(out_h[: int(want_o[-1])].cpu().numpy().view(np.uint64), want,
                                       err_msg=f"{path} replay {rep}")
     assert K.kv_get_last_error() == 0
+
+
+@pytest.mark.parametrize("path", ["table", "two"])
+@pytest.mark.parametrize("n_reqs", [2000, 5000])
+def test_many_requests(n_reqs, path):
+    """More requests than a table CTA keeps offsets for (1024: the slot search reads them from
+    global memory), and more than the table kernel's CTA 0 scans (4096: a separate count launch
+    first); lengths from 0 to 70 tokens at block size 4, shared prefixes among them."""
+    rng = np.random.default_rng(n_reqs)
+    lens = rng.integers(0, 71, size=n_reqs)
+    toks = [rng.integers(-2 ** 31, 2 ** 31, size=int(n), dtype=np.int64).astype(np.int32) for n in lens]
+    for i in range(1, n_reqs, 7):  # every seventh request shares the previous one's prefix
+        m = min(len(toks[i]), len(toks[i - 1]))
+        toks[i][:m] = toks[i - 1][:m]
+    off, flat = W.csr(toks)
+    want_o, want = oracle.block_hashes(off, flat, 4, 123)
+    got_o, got = _gpu(off, flat, 4, 123, path)
+    np.testing.assert_array_equal(got_o, want_o)
+    np.testing.assert_array_equal(got, want)
+    assert K.kv_get_last_error() == 0
